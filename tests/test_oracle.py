@@ -1,0 +1,220 @@
+"""Pins for the CPU oracle: what the pages and the mathematics fix.
+
+Each check ties the oracle to something other than itself: the worked example
+printed in "用 CuTe 读懂 FlashAttention：一次 forward 的完整流程" (Fig. 5-12), the
+causal variant of Fig. 11, closed forms, invariants of softmax attention, a
+library softmax / log-sum-exp, and brute force in 50-digit arithmetic.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.golden import fixtures
+
+EXACT = 1e-14
+
+
+def _ex():
+    return fixtures.load("worked_example.txt")
+
+
+def test_worked_example_plain_definition():
+    ex = _ex()
+    o, lse = oracle.attention(ex["Q"], ex["K"], ex["V"], ex["scale"])
+    np.testing.assert_allclose(o, ex["O"], rtol=0, atol=EXACT)
+    np.testing.assert_allclose(lse, ex["LSE"], rtol=0, atol=EXACT)
+
+
+def test_worked_example_recurrence_intermediates():
+    ex = _ex()
+    o, lse, tr = oracle.blocked_head(ex["Q"], ex["K"], ex["V"], ex["scale"], False,
+                                     int(ex["block_n"]), trace=True)
+    # round 0 (Fig. 6, Fig. 8, l0 = 3/2, m = 1); no rescale on the first block
+    np.testing.assert_allclose(tr["m"][0], ex["m0"], atol=EXACT)
+    np.testing.assert_allclose(tr["e"][0], ex["E0"], atol=EXACT)
+    np.testing.assert_allclose(tr["l"][0], ex["l0"], atol=EXACT)
+    np.testing.assert_allclose(tr["u"][0], ex["U0"], atol=EXACT)
+    assert np.all(np.isnan(tr["alpha"][0]))
+    # round 1 (alpha = 1/2, Fig. 7, l1, Fig. 9, Fig. 10)
+    np.testing.assert_allclose(tr["m"][1], ex["m1"], atol=EXACT)
+    np.testing.assert_allclose(tr["alpha"][1], ex["alpha1"], atol=EXACT)
+    np.testing.assert_allclose(tr["e"][1], ex["E1"], atol=EXACT)
+    np.testing.assert_allclose(tr["l"][1], ex["l1"], atol=EXACT)
+    np.testing.assert_allclose(tr["u"][1], ex["U1"], atol=EXACT)
+    du = tr["u"][1] - tr["alpha"][1][:, None] * tr["u"][0]
+    np.testing.assert_allclose(du, ex["dU1"], atol=EXACT)
+    # raw scores of Fig. 5 recovered from the weights: e = 2^(x - m) when s = ln 2
+    s_rec = np.concatenate([np.log2(tr["e"][t]) + tr["m"][t][:, None] for t in range(2)],
+                           axis=1)
+    np.testing.assert_allclose(s_rec, ex["S"], atol=1e-12)
+    np.testing.assert_allclose(o, ex["O"], atol=EXACT)
+    np.testing.assert_allclose(lse, ex["LSE"], atol=EXACT)
+
+
+def test_worked_example_causal():
+    ex = _ex()
+    cz = fixtures.load("worked_example_causal.txt")
+    o, lse = oracle.attention(ex["Q"], ex["K"], ex["V"], cz["scale"], causal=True)
+    np.testing.assert_allclose(o, cz["O"], atol=EXACT)
+    np.testing.assert_allclose(lse, cz["LSE"], atol=EXACT)
+    ob, lseb, tr = oracle.blocked_head(ex["Q"], ex["K"], ex["V"], cz["scale"], True,
+                                       int(cz["block_n"]), trace=True)
+    np.testing.assert_allclose(ob, cz["O"], atol=EXACT)
+    np.testing.assert_allclose(lseb, cz["LSE"], atol=EXACT)
+    # Fig. 11: masked positions carry no weight; the future block is skipped
+    masked = np.isinf(cz["S_causal"][:, :2])
+    assert np.all(tr["e"][0][masked] == 0.0)
+    k = int(cz["skipped_block"])
+    assert np.all(tr["e"][k] == 0.0) and np.all(np.isnan(tr["alpha"][k]))
+    np.testing.assert_array_equal(tr["l"][k], tr["l"][0])
+
+
+def _rand_case(rng, n, d, scale_hi=1.5):
+    q = rng.standard_normal((n, d))
+    k = rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    s = float(rng.uniform(0.05, scale_hi))
+    return q, k, v, s
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_recurrence_equals_plain_definition_for_every_block_size(causal):
+    rng = np.random.default_rng(11)
+    for n in range(1, 10):
+        for d in (1, 2, 3, 5):
+            q, k, v, s = _rand_case(rng, n, d)
+            o_ref, lse_ref = oracle.attention(q, k, v, s, causal)
+            for bn in range(1, n + 2):
+                o, lse = oracle.blocked_head(q, k, v, s, causal, bn)
+                np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probabilities_match_library_softmax_and_sum_to_one(causal):
+    from scipy.special import logsumexp, softmax
+    rng = np.random.default_rng(5)
+    n = 7
+    q, k, _, s = _rand_case(rng, n, n)
+    v = np.eye(n)                       # O row i is then the probability row P_i
+    p, lse = oracle.attention(q, k, v, s, causal)
+    scores = s * (q @ k.T)
+    for i in range(n):
+        nv = i + 1 if causal else n
+        np.testing.assert_allclose(p[i, :nv], softmax(scores[i, :nv]), atol=1e-14)
+        np.testing.assert_allclose(p[i, nv:], 0.0, atol=0)
+        assert abs(p[i].sum() - 1.0) < 1e-14
+        assert abs(lse[i] - logsumexp(scores[i, :nv])) < 1e-13
+
+
+def test_key_permutation_invariance_noncausal():
+    rng = np.random.default_rng(7)
+    q, k, v, s = _rand_case(rng, 9, 4)
+    o, lse = oracle.attention(q, k, v, s)
+    perm = rng.permutation(9)
+    o2, lse2 = oracle.attention(q, k[perm], v[perm], s)
+    np.testing.assert_allclose(o2, o, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_convex_combination_and_lse_bounds(causal):
+    rng = np.random.default_rng(3)
+    q, k, v, s = _rand_case(rng, 12, 6)
+    o, lse = oracle.attention(q, k, v, s, causal)
+    x = q @ k.T
+    for i in range(12):
+        nv = i + 1 if causal else 12
+        lo, hi = v[:nv].min(axis=0), v[:nv].max(axis=0)
+        assert np.all(o[i] >= lo - 1e-14) and np.all(o[i] <= hi + 1e-14)
+        m = x[i, :nv].max()
+        assert s * m - 1e-14 <= lse[i] <= s * m + math.log(nv) + 1e-14
+
+
+def test_single_key_gives_value_row():
+    rng = np.random.default_rng(9)
+    q, k, v, s = _rand_case(rng, 1, 8)
+    o, lse = oracle.attention(q, k, v, s)
+    np.testing.assert_array_equal(o, v)
+    assert abs(lse[0] - s * float(q[0] @ k[0])) < 1e-14
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_give_uniform_weights(causal):
+    rng = np.random.default_rng(13)
+    _, k, v, s = _rand_case(rng, 10, 3)
+    q = np.zeros_like(k)
+    o, lse = oracle.attention(q, k, v, s, causal)
+    for i in range(10):
+        nv = i + 1 if causal else 10
+        np.testing.assert_allclose(o[i], v[:nv].mean(axis=0), atol=1e-14)
+        assert abs(lse[i] - math.log(nv)) < 1e-14
+
+
+def test_constant_values_give_constant_output():
+    rng = np.random.default_rng(17)
+    q, k, _, s = _rand_case(rng, 8, 5)
+    c = rng.standard_normal(5)
+    v = np.tile(c, (8, 1))
+    for causal in (False, True):
+        o, _ = oracle.attention(q, k, v, s, causal)
+        np.testing.assert_allclose(o, np.tile(c, (8, 1)), atol=1e-14)
+
+
+def test_dominant_key_selects_its_value():
+    rng = np.random.default_rng(19)
+    q, k, v, _ = _rand_case(rng, 6, 4)
+    k[4] = 40.0 * q[2] / np.linalg.norm(q[2]) ** 2      # q2 . k4 = 40, others O(1)
+    o, _ = oracle.attention(q, k, v, 1.0)
+    np.testing.assert_allclose(o[2], v[4], atol=1e-12)
+
+
+def test_brute_force_fifty_digits():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(23)
+    for n, d, causal in [(1, 1, False), (3, 2, True), (5, 4, False), (8, 3, True), (7, 4, False)]:
+        q, k, v, s = _rand_case(rng, n, d, scale_hi=3.0)
+        o, lse = oracle.attention(q, k, v, s, causal)
+        for i in range(n):
+            nv = i + 1 if causal else n
+            xs = [mpmath.fsum(mpmath.mpf(q[i, c]) * mpmath.mpf(k[j, c]) for c in range(d))
+                  for j in range(nv)]
+            ws = [mpmath.exp(mpmath.mpf(s) * x) for x in xs]     # no max subtraction
+            tot = mpmath.fsum(ws)
+            for c in range(d):
+                ref = mpmath.fsum(w * mpmath.mpf(v[j, c]) for j, w in enumerate(ws)) / tot
+                assert abs(float(ref) - o[i, c]) < 1e-13
+            assert abs(float(mpmath.log(tot)) - lse[i]) < 1e-13
+
+
+def test_decode16_exhaustive_against_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f16 = oracle.decode16(bits, oracle.FP16)
+    ref16 = bits.view(np.float16).astype(np.float64)
+    same = (f16 == ref16) | (np.isnan(f16) & np.isnan(ref16))
+    assert same.all()
+    b16 = oracle.decode16(bits, oracle.BF16)
+    with np.errstate(invalid="ignore"):
+        refb = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    same = (b16 == refb) | (np.isnan(b16) & np.isnan(refb))
+    assert same.all()
+
+
+@pytest.mark.parametrize("dtype", [oracle.FP16, oracle.BF16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows16_matches_widened_definition(dtype, causal):
+    from online_softmax_tiling_gb300 import synth
+    B, H, N, d = 1, 3, 37, 16
+    q = synth.tensor_bits(91, (B, H, N, d), dtype)
+    k = synth.tensor_bits(92, (B, H, N, d), dtype)
+    v = synth.tensor_bits(93, (B, H, N, d), dtype)
+    s = 0.25
+    o_all, lse_all = oracle.attention(oracle.decode16(q, dtype), oracle.decode16(k, dtype),
+                                      oracle.decode16(v, dtype), s, causal)
+    rows = np.array([0, 5, N - 1, N, 2 * N + 17, 3 * N - 1, 40], dtype=np.int64)
+    o, lse = oracle.attention_rows16(q, k, v, dtype, s, causal, rows, nthreads=3)
+    np.testing.assert_array_equal(o, o_all.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(lse, lse_all.reshape(-1)[rows])
