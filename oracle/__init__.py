@@ -72,7 +72,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_f64.restype = ctypes.c_int
     lib.oracle_attention_rows16.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64,
                                             ctypes.c_double, ctypes.c_int, i64p, i64,
-                                            dp, dp, ctypes.c_int]
+                                            dp, dp, dp, ctypes.c_int]
     lib.oracle_attention_rows16.restype = ctypes.c_int
     lib.oracle_blocked_head.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double,
                                         ctypes.c_int, i64, dp, dp, dp, dp, dp, dp, dp]
@@ -126,12 +126,14 @@ def attention(q, k, v, scale: float, causal: bool = False, lib: ctypes.CDLL | No
 
 
 def attention_rows16(q16, k16, v16, dtype: int, scale: float, causal: bool, rows,
-                     nthreads: int | None = None, lib: ctypes.CDLL | None = None):
+                     nthreads: int | None = None, with_spread: bool = False,
+                     lib: ctypes.CDLL | None = None):
     """Plain definition for selected query rows of 16-bit inputs.
 
     q16, k16, v16: uint16 bit patterns of shape [B, H, N, d] (or [BH, N, d]).
     rows: flat row indices ``bh * N + i``.  Returns (O [nrows, d], LSE [nrows])
-    in float64.
+    in float64, plus spread [nrows, d] = sum_j P_ij |v_jc - O_ic| when
+    ``with_spread`` (the sensitivity of O to relative errors in the weights).
     """
     lib = lib or load()
     q16 = np.ascontiguousarray(q16, dtype=np.uint16)
@@ -146,6 +148,7 @@ def attention_rows16(q16, k16, v16, dtype: int, scale: float, causal: bool, rows
     srows = np.ascontiguousarray(rows[order])
     o = np.empty((srows.size, d), dtype=np.float64)
     lse = np.empty(srows.size, dtype=np.float64)
+    spread = np.empty((srows.size, d), dtype=np.float64) if with_spread else None
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
     rc = lib.oracle_attention_rows16(_ptr(q16, ctypes.c_uint16), _ptr(k16, ctypes.c_uint16),
@@ -153,13 +156,17 @@ def attention_rows16(q16, k16, v16, dtype: int, scale: float, causal: bool, rows
                                      float(scale), int(bool(causal)),
                                      _ptr(srows, ctypes.c_int64), srows.size,
                                      _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
-                                     int(nthreads))
+                                     _ptr(spread, ctypes.c_double), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_rows16 failed ({rc})")
     out_o = np.empty_like(o)
     out_lse = np.empty_like(lse)
     out_o[order] = o
     out_lse[order] = lse
+    if with_spread:
+        out_s = np.empty_like(spread)
+        out_s[order] = spread
+        return out_o, out_lse, out_s
     return out_o, out_lse
 
 

@@ -94,14 +94,23 @@ void oracle_decode16(const uint16_t* src, int dtype, double* dst, int64_t n) {
 
 /* ---- one query row, plain definition -------------------------------------- */
 
-/* q: [d]; k, v: [Nk, d] of one (b, h); x: scratch of Nk doubles. */
+/*
+ * q: [d]; k, v: [Nk, d] of one (b, h); x: scratch of Nk doubles.
+ * spread (optional, [d]): sum_j P_ij |v_jc - O_ic|, the probability-weighted
+ * spread of the values around the output.  It bounds how far O moves when
+ * every weight is perturbed by a relative error of at most u: the change in
+ * O_ic is at most 2u * spread_c / (1 - u).  Test tolerances use it for the
+ * rounding of the weights to 16 bits before the P.V product.
+ */
 static void attend_row(const double* q, const double* k, const double* v,
                        int64_t Nk, int64_t d, double s, int causal, int64_t i,
-                       double* x, double* o_row, double* lse_out) {
+                       double* x, double* o_row, double* lse_out, double* spread) {
     int64_t nvalid = Nk;
     if (causal && i + 1 < nvalid) nvalid = i + 1;
     if (nvalid <= 0) {
         for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+        if (spread)
+            for (int64_t c = 0; c < d; ++c) spread[c] = 0.0;
         *lse_out = -INFINITY;
         return;
     }
@@ -127,6 +136,14 @@ static void attend_row(const double* q, const double* k, const double* v,
     }
     for (int64_t c = 0; c < d; ++c) o_row[c] /= l;
     *lse_out = s * m + log(l);
+    if (spread) {
+        for (int64_t c = 0; c < d; ++c) spread[c] = 0.0;
+        for (int64_t j = 0; j < nvalid; ++j) {
+            double p = exp(s * (x[j] - m)) / l;
+            const double* vj = v + j * d;
+            for (int64_t c = 0; c < d; ++c) spread[c] += p * fabs(vj[c] - o_row[c]);
+        }
+    }
 }
 
 /* ---- double inputs, whole tensors ----------------------------------------- */
@@ -144,7 +161,7 @@ int oracle_attention_f64(const double* q, const double* k, const double* v,
         const double* vh = v + bh * Nk * d;
         for (int64_t i = 0; i < Nq; ++i)
             attend_row(qh + i * d, kh, vh, Nk, d, scale, causal, i, x,
-                       o + (bh * Nq + i) * d, lse + bh * Nq + i);
+                       o + (bh * Nq + i) * d, lse + bh * Nq + i, NULL);
     }
     free(x);
     return 0;
@@ -162,6 +179,7 @@ typedef struct {
     int64_t nrows;
     double* o;             /* [nrows, d] */
     double* lse;           /* [nrows] */
+    double* spread;        /* [nrows, d] or NULL */
     int64_t next;          /* work counter (rows handed out in chunks) */
     pthread_mutex_t lock;
     int failed;
@@ -201,7 +219,8 @@ static void* rows_worker(void* arg) {
             }
             oracle_decode16(job->q + flat * d, job->dtype, qr, d);
             attend_row(qr, kh, vh, N, d, job->scale, job->causal, i, x,
-                       job->o + r * d, job->lse + r);
+                       job->o + r * d, job->lse + r,
+                       job->spread ? job->spread + r * d : NULL);
         }
     }
     free(kh); free(vh); free(qr); free(x);
@@ -210,14 +229,14 @@ static void* rows_worker(void* arg) {
 
 /*
  * q, k, v: [BH, N, d] raw 16-bit patterns of `dtype`.  rows: nrows flat row
- * indices (bh * N + i), each in [0, BH * N).  o: [nrows, d], lse: [nrows].
- * Returns 0 on success.
+ * indices (bh * N + i), each in [0, BH * N).  o: [nrows, d], lse: [nrows],
+ * spread: [nrows, d] or NULL (see attend_row).  Returns 0 on success.
  */
 int oracle_attention_rows16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                             int dtype, int64_t BH, int64_t N, int64_t d,
                             double scale, int causal,
                             const int64_t* rows, int64_t nrows,
-                            double* o, double* lse, int nthreads) {
+                            double* o, double* lse, double* spread, int nthreads) {
     if (BH <= 0 || N <= 0 || d <= 0 || nrows < 0) return 1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) return 1;
     for (int64_t r = 0; r < nrows; ++r)
@@ -227,7 +246,7 @@ int oracle_attention_rows16(const uint16_t* q, const uint16_t* k, const uint16_t
     rows_job_t job;
     job.q = q; job.k = k; job.v = v; job.dtype = dtype;
     job.N = N; job.d = d; job.scale = scale; job.causal = causal;
-    job.rows = rows; job.nrows = nrows; job.o = o; job.lse = lse;
+    job.rows = rows; job.nrows = nrows; job.o = o; job.lse = lse; job.spread = spread;
     job.next = 0; job.failed = 0;
     pthread_mutex_init(&job.lock, NULL);
     pthread_t tids[256];

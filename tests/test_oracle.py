@@ -218,3 +218,29 @@ def test_rows16_matches_widened_definition(dtype, causal):
     o, lse = oracle.attention_rows16(q, k, v, dtype, s, causal, rows, nthreads=3)
     np.testing.assert_array_equal(o, o_all.reshape(-1, d)[rows])
     np.testing.assert_array_equal(lse, lse_all.reshape(-1)[rows])
+
+
+def test_spread_matches_brute_force_and_closed_form():
+    from online_softmax_tiling_gb300 import synth
+    dtype, N, d, s = oracle.BF16, 23, 8, 0.3
+    q = synth.tensor_bits(31, (1, 2, N, d), dtype)
+    k = synth.tensor_bits(32, (1, 2, N, d), dtype)
+    v = synth.tensor_bits(33, (1, 2, N, d), dtype)
+    Q, K, V = (oracle.decode16(t, dtype)[0] for t in (q, k, v))
+    rows = np.arange(2 * N, dtype=np.int64)
+    for causal in (False, True):
+        o, _, spread = oracle.attention_rows16(q, k, v, dtype, s, causal, rows, with_spread=True)
+        for r in rows:
+            h, i = divmod(int(r), N)
+            nv = i + 1 if causal else N
+            x = s * (Q[h, i] @ K[h, :nv].T)
+            p = np.exp(x - x.max())
+            p /= p.sum()
+            want = (p[:, None] * np.abs(V[h, :nv] - o[r][None, :])).sum(0)
+            np.testing.assert_allclose(spread[r], want, rtol=1e-12, atol=1e-15)
+    # two keys with equal scores: weights 1/2 each, spread = |v0 - v1| / 2
+    qq = np.zeros((1, 1, 2, 2), np.uint16)
+    vv = synth.round_to_bits(np.array([[[[1.0, -2.0], [3.0, 0.5]]]]), oracle.FP16)
+    _, _, sp = oracle.attention_rows16(qq, qq, vv, oracle.FP16, 1.0, False, [0, 1],
+                                       with_spread=True)
+    np.testing.assert_allclose(sp, [[1.0, 1.25], [1.0, 1.25]], atol=1e-15)

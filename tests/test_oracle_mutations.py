@@ -17,12 +17,14 @@ from tests.golden import fixtures
 MUTATIONS = {
     "lse_drops_scale": ("*lse_out = s * m + log(l);", "*lse_out = m + log(l);"),
     "exponent_sign": ("double w = exp(s * (x[j] - m));", "double w = exp(s * (m - x[j]));"),
+    "spread_drops_abs": ("spread[c] += p * fabs(vj[c] - o_row[c]);",
+                         "spread[c] += p * (vj[c] - o_row[c]);"),
     "causal_off_by_one": ("if (causal && i + 1 < nvalid) nvalid = i + 1;",
                           "if (causal && i < nvalid) nvalid = i;"),
     "no_normalisation": ("for (int64_t c = 0; c < d; ++c) o_row[c] /= l;",
                          "for (int64_t c = 0; c < d; ++c) o_row[c] /= 1.0;"),
-    "wrong_value_row": ("const double* vj = v + j * d;",
-                        "const double* vj = v + (nvalid - 1 - j) * d;"),
+    "wrong_value_row": ("l += w;\n        const double* vj = v + j * d;",
+                        "l += w;\n        const double* vj = v + (nvalid - 1 - j) * d;"),
     "score_uses_wrong_key": ("const double* kj = k + j * d;",
                              "const double* kj = k + (j == 0 ? 0 : j - 1) * d;"),
     "recurrence_drops_alpha_on_l": ("l *= alpha;", "l *= 1.0;"),
@@ -78,6 +80,12 @@ def _pins(lib) -> list:
     db = oracle.decode16(bits, oracle.BF16, lib=lib)
     check("decode16", np.array_equal(d16, ref16, equal_nan=True)
           and np.array_equal(db, refb, equal_nan=True))
+    from online_softmax_tiling_gb300 import synth
+    v = synth.round_to_bits(np.array([[[[1.0, -2.0], [3.0, 0.5]]]]), oracle.FP16)
+    z = np.zeros((1, 1, 2, 2), np.uint16)
+    _, _, sp = oracle.attention_rows16(z, z, v, oracle.FP16, 1.0, False, [0, 1],
+                                       with_spread=True, lib=lib)
+    check("spread_closed_form", np.allclose(sp, [[1.0, 1.25], [1.0, 1.25]], atol=1e-15))
     return failed
 
 
