@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark: fused attention forward TFLOPS on GB300 (one JSON line on stdout).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+A step is one fa_fwd launch over the whole workload (every (b, h) and every
+query tile: Q tile load, K/V streaming, S = QK^T, mask, online softmax, P.V,
+O = U / l and LSE).  The default workload is B=2, H=32, N=4096, d=128, bf16,
+non-causal: the N=4096, d=128 point at which the throughput target is stated.
+The metric is 4*B*H*N^2*d / t (halved for the causal mask), in TFLOPS, summed
+over ranks.  Inputs are seeded synthetic tensors already resident in HBM; the
+per-step working set (Q, K, V, O: 256 MiB) is larger than the 129 MB L2.
+
+Multi-GPU: one process per GPU (torchrun); the (b, h) units are independent,
+so each rank runs its own batch of heads with no data-path collective (weak
+scaling); only the timing is reduced (max over ranks).
+
+--impl reference times the oracle (the plain double-precision CPU
+definition) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from online_softmax_tiling_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "T_b2h32n4096d128_bf16"
+KERNEL_SOURCES = ["online_softmax_tiling_gb300/csrc/fa_fwd_kernel.cuh",
+                  "online_softmax_tiling_gb300/csrc/sm103_ptx.cuh",
+                  "online_softmax_tiling_gb300/csrc/fa_api.cu"]
+METRIC = "attn fwd TFLOPS (4*B*H*N^2*d/t, causal halved) @N=4096; % of GB300 dense TC peak"
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed_base(w: synth.Workload, rank: int) -> int:
+    """Each rank draws its own independent heads (weak scaling, disjoint units)."""
+    return w.seed_base + 100 * rank
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, khash: str):
+    """DRAM bytes per launch recorded by an ncu capture of this exact kernel source."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    pat = re.compile(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+kernel_hash:\s*([0-9a-f]+)"
+                     r"\s+workload:\s*(\S+)")
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name), encoding="utf-8") as fh:
+            for m in pat.finditer(fh.read()):
+                if m.group(2) == khash and m.group(3) == workload:
+                    return float(m.group(1))
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path, encoding="utf-8") as fh:
+            return json.load(fh), "measured"
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+        self.lines.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in list(self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import online_softmax_tiling_gb300 as fa
+    from online_softmax_tiling_gb300 import build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or world > 1:
+        build.build()
+    barrier(world)
+
+    w = synth.workload(args.workload)
+    B, H, N, d = w.shape
+    q_h, k_h, v_h = synth.make_inputs(w, seed_base=rank_seed_base(w, rank))
+    tdt = torch.float16 if w.dtype == synth.FP16 else torch.bfloat16
+
+    def host(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(tdt).pin_memory()
+
+    qh, kh, vh = host(q_h), host(k_h), host(v_h)
+    q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def step():
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, w.scale, int(w.causal), w.dtype, sptr)
+        if st != fa.FA_OK:
+            raise fa.FaError(st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_check_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t_wall) * 1e3
+    barrier(world)
+    clock_info = clocks.stop()
+    dev_ms = ev0.elapsed_time(ev1)
+    if fa.fa_check_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    ms_total = max_over_ranks(dev_ms, world)
+    ms_per_step = ms_total / args.steps
+    flops_rank = w.flops
+    value = flops_rank * world / (ms_per_step * 1e-3) / 1e12
+
+    # kernel roofline: one launch per step on `stream`, timed by the events above
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops_rank / (dev_ms / args.steps * 1e-3) / 1e12
+    khash = kernel_hash()
+    traffic = profiled_traffic(args.workload, khash)
+
+    # end-to-end through the public API with host buffers: H2D of q, k, v from
+    # pinned memory, the fa_fwd call, D2H of O and LSE, every step
+    o_host = torch.empty(o.shape, dtype=tdt, pin_memory=True)
+    l_host = torch.empty(lse.shape, dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        step()
+        o_host.copy_(o, non_blocking=True)
+        l_host.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * 4
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": synth.DTYPE_NAMES[w.dtype], "data": "synthetic (seeded N(0,1), SplitMix64 + Box-Muller)",
+            "config": {**w.describe(), "parallelism": f"independent heads per rank x{world}",
+                       "l2": "inputs larger than L2: 256 MiB of Q, K, V, O per step vs 129 MB L2",
+                       "pct_of_peak": round(100 * value / world / peak, 2)},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "kernel_hash": khash},
+            "e2e": {"value": round(flops_rank * world / (e2e_ms * 1e-3) / 1e12, 3),
+                    "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clock_info,
+            "wall_ms_timed_region": round(wall_ms, 3),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------- oracle timing
+def _row_flops(w: synth.Workload, rows: np.ndarray) -> float:
+    i = rows % w.N
+    keys = np.minimum(i + 1, w.N) if w.causal else np.full(rows.shape, w.N)
+    return float(4.0 * w.d * keys.sum())
+
+
+def cpu_baseline(w, q_h, k_h, v_h, budget_s: float = 10.0, steps: int = 1):
+    """Time the oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    BH = w.B * w.H
+    # calibrate on a small sample, then size the sample to the time budget
+    probe = synth.sample_rows(BH, w.N, 64, 12345, include_edges=False)
+    t0 = time.perf_counter()
+    oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, probe, nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(64, min(BH * w.N, 64 * budget_s / dt / steps)))
+    total_flops, total_t = 0.0, 0.0
+    for s in range(steps):
+        rows = synth.sample_rows(BH, w.N, n, 777 + s, include_edges=False)
+        t0 = time.perf_counter()
+        oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, rows, nthreads=cores)
+        total_t += time.perf_counter() - t0
+        total_flops += _row_flops(w, rows)
+    return {"value": round(total_flops / total_t / 1e12, 6), "unit": "TFLOPS", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} seeded query rows (all their keys) of {w.name}, fp64, "
+                      f"{total_t:.1f} s on {cores} host threads"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.workload(args.workload)
+    q_h, k_h, v_h = synth.make_inputs(w)
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    BH = w.B * w.H
+    rows_per_step = args.ref_rows
+    for s in range(args.warmup):
+        oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal,
+                                synth.sample_rows(BH, w.N, rows_per_step, 900 + s, False),
+                                nthreads=cores)
+    flops, t = 0.0, 0.0
+    for s in range(args.steps):
+        rows = synth.sample_rows(BH, w.N, rows_per_step, 1900 + s, False)
+        t0 = time.perf_counter()
+        oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, rows, nthreads=cores)
+        t += time.perf_counter() - t0
+        flops += _row_flops(w, rows)
+    value = flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), SplitMix64 + Box-Muller)",
+        "config": {**w.describe(), "parallelism": "host cores (oracle)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded query rows per step of {w.name}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=256)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

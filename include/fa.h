@@ -1,0 +1,102 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The operation ("用 CuTe 读懂 FlashAttention：一次 forward 的完整流程",
+ * section "先固定一个例子", equation S = QK^T, P = softmax_row(sS), O = PV;
+ * "CUDA 算子工程" ch. 14, section 14.1):
+ *
+ *   for each batch b, head h and query row i < N,
+ *     O[b,h,i,:] = sum_j softmax_j(s * q_i . k_j) * v_j
+ *     LSE[b,h,i] = ln sum_j exp(s * q_i . k_j)
+ *   over the keys j < N, and only j <= i when `causal` is non-zero (top-left
+ *   alignment, section "causal 模式在哪一步生效", Fig. 11).  LSE is the
+ *   side output s*m + ln(l) of section "最后：归一化并写回 O".
+ *
+ * The library computes this in one kernel launch, FlashAttention-2 loop
+ * order (one CTA per 128-row query tile, key/value tiles streamed through
+ * shared memory, scores and weights kept in tensor memory, never in HBM).
+ *
+ * This header needs no CUDA header: streams are passed as void*.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define FA_OK 0               /* success (for fa_fwd: validated and enqueued)            */
+#define FA_ERR_INVALID_ARG 1  /* null pointer, non-positive size, bad dtype, bad scale    */
+#define FA_ERR_UNSUPPORTED 2  /* valid request outside the compiled set (head dim d)      */
+#define FA_ERR_MISALIGNED 3   /* q, k, v or o not 16-byte aligned; lse not 4-byte aligned */
+#define FA_ERR_CUDA 4         /* a CUDA runtime/driver call failed (launch, encode, sync) */
+#define FA_ERR_TIMEOUT 5      /* a pipeline wait inside the kernel ran out of time        */
+
+/* Element types of q, k, v and o. */
+#define FA_FP16 0             /* IEEE binary16 */
+#define FA_BF16 1             /* bfloat16      */
+
+/*
+ * fa_fwd - fused scaled-dot-product attention forward with log-sum-exp.
+ *
+ * q, k, v : device pointers, [B, H, N, d] contiguous (row-major, d fastest),
+ *           element type `dtype`.  Read only.
+ * o       : device pointer, [B, H, N, d] contiguous, element type `dtype`.
+ *           Written: every row i < N of every (b, h).  O is the exact softmax
+ *           average of the 16-bit-rounded weights, rounded to nearest even.
+ * lse     : device pointer, [B, H, N] contiguous float32.  Written: the natural
+ *           log-sum-exp of the scaled scores of each row.
+ * B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1.
+ *           B*H and N must each fit the TMA tensor map (< 2^31).
+ * d       : head dimension; 64 or 128 (anything else: FA_ERR_UNSUPPORTED).
+ * scale   : the softmax scale s (for the standard definition 1/sqrt(d)); must
+ *           be finite and > 0.  There is no default.
+ * causal  : 0 = full attention, non-zero = key j visible to query i iff j <= i.
+ * dtype   : FA_FP16 or FA_BF16.
+ * stream  : cudaStream_t to enqueue on (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns all buffers; the library allocates no device
+ * memory per call and keeps no pointer after the call returns.  q, k, v must
+ * not overlap o or lse.
+ * Asynchrony: the kernel is enqueued on `stream`; the return value covers
+ * argument checks, tensor-map encoding and the launch itself.  Errors inside
+ * the kernel (a pipeline wait that timed out) are reported by
+ * fa_check_device_status().
+ * Thread safety: safe to call concurrently from several host threads.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, int dtype,
+           void* stream);
+
+/*
+ * fa_check_device_status - synchronise `stream`, then return and clear the
+ * device-side status word: FA_OK, FA_ERR_TIMEOUT (some CTA's bounded wait
+ * expired and that CTA left its outputs unwritten), or FA_ERR_CUDA if the
+ * synchronisation itself failed.  The status word is shared by all launches
+ * on the current device.
+ */
+int fa_check_device_status(void* stream);
+
+/* fa_status_string - static, human-readable name of a status code. */
+const char* fa_status_string(int status);
+
+/* fa_version - library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+/*
+ * fa_fwd_debug - fa_fwd with testing controls; not for production use.
+ * fault_mode : 0 = none; 1 = the loader never issues the first key tile, so
+ *              the tensor-core warp's wait for it must time out, set
+ *              FA_ERR_TIMEOUT and let every CTA exit cleanly.
+ * timeout_s  : limit of every pipeline wait, in seconds (> 0; fa_fwd uses 2 s).
+ */
+int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal, int dtype,
+                 void* stream, int fault_mode, double timeout_s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

@@ -1,1 +1,128 @@
-"""GB300-native fused attention forward (online-softmax tiling)."""
+"""GB300-native fused attention forward (online-softmax tiling), Python binding.
+
+Argument marshalling only: every step of the computation runs in the sm_103a
+kernels of ``libfa_gb300.so`` behind the C ABI of ``include/fa.h``.  The names
+follow that header: ``fa_fwd``, ``fa_check_device_status``,
+``fa_status_string``, ``fa_version`` and ``fa_fwd_debug``.  There is no CPU
+fallback: if the library is missing, the first call raises.
+
+``attention_forward`` is a convenience wrapper over ``fa_fwd`` for torch
+tensors; torch is used only to allocate device memory and to name the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, FA_ERR_TIMEOUT = (
+    0, 1, 2, 3, 4, 5)
+FA_FP16, FA_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
+EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str = "fa_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {fa_status_string(status)} ({status})")
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C-ABI library (built by ``online_softmax_tiling_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise FileNotFoundError(
+                    f"{LIBRARY} is missing: build it with "
+                    "`python -m online_softmax_tiling_gb300.build` (there is no CPU fallback)")
+            lib = ctypes.CDLL(LIBRARY)
+            vp, i = ctypes.c_void_p, ctypes.c_int
+            lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, i, vp]
+            lib.fa_fwd.restype = i
+            lib.fa_fwd_debug.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, i, vp,
+                                         i, ctypes.c_double]
+            lib.fa_fwd_debug.restype = i
+            lib.fa_check_device_status.argtypes = [vp]
+            lib.fa_check_device_status.restype = i
+            lib.fa_status_string.argtypes = [i]
+            lib.fa_status_string.restype = ctypes.c_char_p
+            lib.fa_version.argtypes = []
+            lib.fa_version.restype = i
+            _lib = lib
+        return _lib
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream) -> int:
+    """Raw C call: q, k, v, o, lse and stream are integer addresses (or None)."""
+    return library().fa_fwd(q, k, v, o, lse, int(B), int(H), int(N), int(d), float(scale),
+                            int(causal), int(dtype), stream)
+
+
+def fa_fwd_debug(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, fault_mode,
+                 timeout_s) -> int:
+    return library().fa_fwd_debug(q, k, v, o, lse, int(B), int(H), int(N), int(d), float(scale),
+                                  int(causal), int(dtype), stream, int(fault_mode),
+                                  float(timeout_s))
+
+
+def fa_check_device_status(stream=None) -> int:
+    return library().fa_check_device_status(stream)
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return library().fa_status_string(int(status)).decode()
+    except FileNotFoundError:
+        return f"status {status}"
+
+
+def fa_version() -> int:
+    return library().fa_version()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float16 or bfloat16)")
+
+
+def attention_forward(q, k, v, scale: float | None = None, causal: bool = False, out=None,
+                      lse=None, stream=None):
+    """O, LSE for contiguous CUDA tensors q, k, v of shape [B, H, N, d].
+
+    scale defaults to 1/sqrt(d).  Outputs are allocated with torch unless
+    given.  Raises FaError on any non-OK status.  Asynchronous on `stream`
+    (default: torch's current stream).
+    """
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must be [B, H, N, d] of one shape")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                N, d, scale, causal, _dtype_code(q), handle)
+    if st != FA_OK:
+        raise FaError(st)
+    return out, lse

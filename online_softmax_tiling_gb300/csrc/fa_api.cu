@@ -1,0 +1,193 @@
+// fa_api.cu - host side of the C ABI declared in include/fa.h: argument
+// checks, TMA tensor-map encoding, kernel selection and launch.
+//
+// The problem statement it validates is that of "CUDA 算子工程" ch. 14,
+// section 14.5 (inputs Q, K, V [N, d]; outputs O [N, d] and LSE [N]), per
+// (batch, head), with the explicit scale and causal flag of
+// "用 CuTe 读懂 FlashAttention：一次 forward 的完整流程" (sections
+// "先固定一个例子" and "causal 模式在哪一步生效").
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [B*H, N, d] 16-bit tensor viewed in 3-D so that rows >= N of one head are
+// out of range (zero-filled on load, clipped on store) instead of belonging
+// to the next head.  Box: 64 columns (128 bytes, one swizzle span) x 128 rows.
+bool encode_qkvo(CUtensorMap* map, const void* ptr, int dtype, int64_t BH, int64_t N, int64_t d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, fa::FwdParams);
+
+template <int D, bool BF16, bool CAUSAL>
+KernelFn kernel_of() {
+    return reinterpret_cast<KernelFn>(&fa::fa_fwd_kernel<D, BF16, CAUSAL>);
+}
+
+struct KernelEntry {
+    const void* fn;
+    int smem;
+};
+
+KernelEntry select_kernel(int d, int dtype, bool causal) {
+#define FA_ENTRY(D, BF, CA) \
+    KernelEntry { reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF, CA>), fa::Cfg<D>::kSmemBytes }
+    const bool bf = dtype == FA_BF16;
+    if (d == 64) {
+        if (bf) return causal ? FA_ENTRY(64, true, true) : FA_ENTRY(64, true, false);
+        return causal ? FA_ENTRY(64, false, true) : FA_ENTRY(64, false, false);
+    }
+    if (bf) return causal ? FA_ENTRY(128, true, true) : FA_ENTRY(128, true, false);
+    return causal ? FA_ENTRY(128, false, true) : FA_ENTRY(128, false, false);
+#undef FA_ENTRY
+}
+
+// Opt each kernel into its dynamic shared memory once per device.
+bool ensure_smem_attr(const void* fn, int smem, int device) {
+    static std::mutex mu;
+    static std::atomic<uint64_t> done_mask[8][64];  // [kernel slot][device / 64 word]
+    static const void* slots[8] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < 8; ++i) {
+        if (slots[i] == fn) { slot = i; break; }
+        if (slots[i] == nullptr) { slots[i] = fn; slot = i; break; }
+    }
+    if (slot < 0 || device < 0 || device >= 64 * 64) return false;
+    const uint64_t bit = 1ull << (device & 63);
+    if (done_mask[slot][device >> 6].load() & bit) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return false;
+    done_mask[slot][device >> 6].fetch_or(bit);
+    return true;
+}
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, int dtype, void* stream, int fault_mode,
+             double timeout_s) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!(timeout_s > 0.0) || !std::isfinite(timeout_s)) return FA_ERR_INVALID_ARG;
+    if (fault_mode < 0 || fault_mode > 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const int64_t nq = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
+    auto misaligned = [](const void* ptr, uintptr_t a) {
+        return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+    };
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+        misaligned(lse, 4))
+        return FA_ERR_MISALIGNED;
+
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_qkvo(&tq, q, dtype, BH, N, d) || !encode_qkvo(&tk, k, dtype, BH, N, d) ||
+        !encode_qkvo(&tv, v, dtype, BH, N, d) || !encode_qkvo(&to, o, dtype, BH, N, d))
+        return FA_ERR_CUDA;
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+    const KernelEntry ke = select_kernel(d, dtype, causal != 0);
+    if (!ensure_smem_attr(ke.fn, ke.smem, device)) return FA_ERR_CUDA;
+
+    fa::FwdParams prm;
+    prm.lse = lse;
+    prm.N = N;
+    prm.num_q_tiles = static_cast<int>(nq);
+    prm.scale = scale;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    prm.timeout_ns = static_cast<unsigned long long>(timeout_s * 1e9);
+    prm.fault_mode = fault_mode;
+
+    void* args[] = {&tq, &tk, &tv, &to, &prm};
+    const dim3 grid(static_cast<unsigned>(BH * nq));
+    const dim3 block(fa::kThreads);
+    if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem),
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, int dtype, void* stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0);
+}
+
+int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, int dtype, void* stream, int fault_mode,
+                 double timeout_s) {
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, fault_mode,
+                    timeout_s);
+}
+
+int fa_check_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int st = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&st, fa::g_fa_status, sizeof(st)) != cudaSuccess) return FA_ERR_CUDA;
+    if (st != 0 && cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(zero)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return static_cast<int>(st);
+}
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+"""Shared helpers for the GPU parity tests: upload seeded inputs, run the CUDA
+path through the C ABI, compare with the oracle under the stated tolerance.
+
+Tolerance (applied per output element, "Tolerance"):
+  * the stated bounds are max |dO| <= 4e-3, mean |dO| <= 5e-4 for 16-bit O and
+    |dLSE| <= 1e-4 relative for fp32 LSE;
+  * O is a 16-bit value, so rounding the exact result to the output type is
+    unavoidable: the error is measured beyond half an ulp of the output type
+    ("excess");
+  * the pages prescribe rounding the weights P to the 16-bit input type before
+    the P.V product.  With O normalised by the sum of those same rounded
+    weights, a relative rounding error of at most u in every weight moves O_ic
+    by at most u / (1 - u) * sum_j P_ij |v_jc - O_ic| (the oracle's "spread").
+    The max gate is applied to the error beyond both roundings; the mean gate
+    to the error beyond the output rounding alone;
+  * relative LSE error uses max(1, |LSE|) as the denominator (LSE can be ~0).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import oracle
+from online_softmax_tiling_gb300 import synth
+
+MAX_EXCESS = 4e-3
+MEAN_EXCESS = 5e-4
+LSE_REL = 1e-4
+UNIT_ROUNDOFF = {synth.FP16: 2.0 ** -11, synth.BF16: 2.0 ** -8}
+PRECISION = {synth.FP16: 11, synth.BF16: 8}
+
+
+def to_device(bits: np.ndarray, dtype: int, device="cuda"):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    t = t.view(torch.float16 if dtype == synth.FP16 else torch.bfloat16)
+    return t.to(device)
+
+
+def from_device(t) -> np.ndarray:
+    import torch
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def half_ulp(x: np.ndarray, dtype: int) -> np.ndarray:
+    _, e = np.frexp(np.abs(x))
+    return 0.5 * np.ldexp(1.0, np.maximum(e - PRECISION[dtype],
+                                          -24 if dtype == synth.FP16 else -133))
+
+
+def compare(o_bits, lse, o_ref, lse_ref, spread, dtype):
+    """Error statistics of GPU rows (o_bits: uint16 [n, d], lse: [n]) vs the oracle."""
+    o = synth.bits_to_float(o_bits, dtype).astype(np.float64)
+    raw = np.abs(o - o_ref)
+    hu = half_ulp(np.maximum(np.abs(o), np.abs(o_ref)), dtype)
+    u = UNIT_ROUNDOFF[dtype]
+    allow = u / (1 - u) * spread + 1e-5 * (np.abs(o_ref) + spread)
+    excess = np.maximum(0.0, raw - hu)
+    excess_p = np.maximum(0.0, raw - hu - allow)
+    dl = np.abs(lse.astype(np.float64) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    return {
+        "raw_max": float(raw.max()), "raw_mean": float(raw.mean()),
+        "excess_max": float(excess.max()), "excess_mean": float(excess.mean()),
+        "excess_beyond_weight_rounding_max": float(excess_p.max()),
+        "n_excess_over_max": int((excess > MAX_EXCESS).sum()),
+        "lse_rel_max": float(dl.max()), "finite": bool(np.isfinite(o).all() and
+                                                        np.isfinite(lse).all()),
+    }
+
+
+def assert_within(stats: dict, label: str = ""):
+    assert stats["finite"], f"{label}: non-finite output {stats}"
+    assert stats["excess_beyond_weight_rounding_max"] <= MAX_EXCESS, f"{label}: {stats}"
+    assert stats["excess_mean"] <= MEAN_EXCESS, f"{label}: {stats}"
+    assert stats["lse_rel_max"] <= LSE_REL, f"{label}: {stats}"
+
+
+def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0):
+    """Run fa_fwd on uploaded inputs; returns (o_bits [B,H,N,d], lse [B,H,N], guards ok)."""
+    import torch
+    import online_softmax_tiling_gb300 as fa
+    B, H, N, d = q_bits.shape
+    q, k, v = (to_device(x, dtype) for x in (q_bits, k_bits, v_bits))
+    n_o = B * H * N * d
+    tdt = torch.float16 if dtype == synth.FP16 else torch.bfloat16
+    # guard bands before and after O and LSE, filled with a canary pattern
+    o_buf = torch.full((n_o + 2 * guard,), -7777.0, dtype=tdt, device="cuda")
+    l_buf = torch.full((B * H * N + 2 * guard,), -7777.0, dtype=torch.float32, device="cuda")
+    o = o_buf[guard:guard + n_o].view(B, H, N, d)
+    lse = l_buf[guard:guard + B * H * N].view(B, H, N)
+    stream = torch.cuda.current_stream()
+    st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                   B, H, N, d, scale, int(causal), dtype, stream.cuda_stream)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    assert fa.fa_check_device_status(stream.cuda_stream) == fa.FA_OK
+    guards_ok = True
+    if guard:
+        ob = o_buf.float().cpu().numpy()
+        lb = l_buf.cpu().numpy()
+        guards_ok = bool((ob[:guard] == -7777.0).all() and (ob[guard + n_o:] == -7777.0).all()
+                         and (lb[:guard] == -7777.0).all()
+                         and (lb[guard + B * H * N:] == -7777.0).all())
+    return from_device(o), lse.cpu().numpy(), guards_ok
+
+
+def oracle_rows(q_bits, k_bits, v_bits, dtype, scale, causal, rows):
+    return oracle.attention_rows16(q_bits, k_bits, v_bits, dtype, scale, causal, rows,
+                                   with_spread=True)

@@ -1,0 +1,82 @@
+"""The C-ABI library loads, exports what include/fa.h declares, and rejects bad
+arguments on the host (no GPU needed: these paths return before any CUDA call)."""
+import os
+import re
+
+import pytest
+
+import online_softmax_tiling_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "fa.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIBRARY):
+        from online_softmax_tiling_gb300 import build
+        build.build()
+    return fa.library()
+
+
+def test_header_declares_the_exports():
+    assert _declared() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert fa.fa_version() >= 100
+    names = [fa.fa_status_string(s) for s in range(6)]
+    assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+                     "FA_ERR_CUDA", "FA_ERR_TIMEOUT"]
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced "device" addresses: every call below fails validation.
+A = 0x10000
+
+
+def _call(**kw):
+    args = dict(q=A, k=A + 0x1000, v=A + 0x2000, o=A + 0x3000, lse=A + 0x4000, B=1, H=1, N=128,
+                d=64, scale=0.125, causal=0, dtype=fa.FA_FP16, stream=None)
+    args.update(kw)
+    return fa.fa_fwd(**args)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=0), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, kw, want):
+    assert _call(**kw) == want
+
+
+def test_debug_entry_validates_its_controls(lib):
+    base = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 1, 128, 64, 0.125, 0,
+            fa.FA_FP16, None)
+    assert fa.fa_fwd_debug(*base, 2, 1.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_debug(*base, 0, 0.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_debug(*base, 0, float("nan")) == fa.FA_ERR_INVALID_ARG
