@@ -133,7 +133,7 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         t0 = time.time()
-        while not self.lines and time.time() - t0 < 5:
+        while not self.lines and time.time() - t0 < 10:
             time.sleep(0.02)
         self.lines.clear()
 
@@ -305,27 +305,25 @@ def _row_flops(w: synth.Workload, rows: np.ndarray) -> float:
     return float(4.0 * w.d * keys.sum())
 
 
-def cpu_baseline(w, q_h, k_h, v_h, budget_s: float = 10.0, steps: int = 1):
+def cpu_baseline(w, q_h, k_h, v_h, budget_s: float = 10.0):
     """Time the oracle (as it stands) on a bounded row sample of the workload."""
     import oracle
     cores = len(os.sched_getaffinity(0))
     BH = w.B * w.H
     # calibrate on a small sample, then size the sample to the time budget
-    probe = synth.sample_rows(BH, w.N, 64, 12345, include_edges=False)
-    t0 = time.perf_counter()
-    oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, probe, nthreads=cores)
-    dt = max(time.perf_counter() - t0, 1e-3)
-    n = int(max(64, min(BH * w.N, 64 * budget_s / dt / steps)))
-    total_flops, total_t = 0.0, 0.0
-    for s in range(steps):
-        rows = synth.sample_rows(BH, w.N, n, 777 + s, include_edges=False)
+    chunk = 16 * cores
+    total_flops, total_t, nrows, s = 0.0, 0.0, 0, 0
+    while total_t < budget_s and nrows < BH * w.N:
+        rows = synth.sample_rows(BH, w.N, chunk, 777 + s, include_edges=False)
         t0 = time.perf_counter()
         oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, rows, nthreads=cores)
         total_t += time.perf_counter() - t0
         total_flops += _row_flops(w, rows)
+        nrows += rows.size
+        s += 1
     return {"value": round(total_flops / total_t / 1e12, 6), "unit": "TFLOPS", "cores": cores,
             "kind": "oracle",
-            "sample": f"{n} seeded query rows (all their keys) of {w.name}, fp64, "
+            "sample": f"{nrows} seeded query rows (all their keys) of {w.name}, fp64, "
                       f"{total_t:.1f} s on {cores} host threads"}
 
 
@@ -370,7 +368,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

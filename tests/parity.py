@@ -85,8 +85,8 @@ def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0):
     n_o = B * H * N * d
     tdt = torch.float16 if dtype == synth.FP16 else torch.bfloat16
     # guard bands before and after O and LSE, filled with a canary pattern
-    o_buf = torch.full((n_o + 2 * guard,), -7777.0, dtype=tdt, device="cuda")
-    l_buf = torch.full((B * H * N + 2 * guard,), -7777.0, dtype=torch.float32, device="cuda")
+    o_buf = torch.full((n_o + 2 * guard,), -1000.0, dtype=tdt, device="cuda")
+    l_buf = torch.full((B * H * N + 2 * guard,), -1000.0, dtype=torch.float32, device="cuda")
     o = o_buf[guard:guard + n_o].view(B, H, N, d)
     lse = l_buf[guard:guard + B * H * N].view(B, H, N)
     stream = torch.cuda.current_stream()
@@ -98,9 +98,9 @@ def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0):
     if guard:
         ob = o_buf.float().cpu().numpy()
         lb = l_buf.cpu().numpy()
-        guards_ok = bool((ob[:guard] == -7777.0).all() and (ob[guard + n_o:] == -7777.0).all()
-                         and (lb[:guard] == -7777.0).all()
-                         and (lb[guard + B * H * N:] == -7777.0).all())
+        guards_ok = bool((ob[:guard] == -1000.0).all() and (ob[guard + n_o:] == -1000.0).all()
+                         and (lb[:guard] == -1000.0).all()
+                         and (lb[guard + B * H * N:] == -1000.0).all())
     return from_device(o), lse.cpu().numpy(), guards_ok
 
 
