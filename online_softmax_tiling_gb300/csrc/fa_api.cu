@@ -40,7 +40,8 @@ EncodeTiledFn encode_fn() {
 
 // [B*H, N, d] 16-bit tensor viewed in 3-D so that rows >= N of one head are
 // out of range (zero-filled on load, clipped on store) instead of belonging
-// to the next head.  Box: 64 columns (128 bytes, one swizzle span) x 128 rows.
+// to the next head.  Box: 64 columns (128 bytes, one swizzle span) x 128 rows
+// (one query tile, one key tile).
 bool encode_qkvo(CUtensorMap* map, const void* ptr, int dtype, int64_t BH, int64_t N, int64_t d) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -113,7 +114,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (fault_mode < 0 || fault_mode > 1) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    const int64_t nq = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    const int64_t nq = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;  // CTAs per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
     auto misaligned = [](const void* ptr, uintptr_t a) {
         return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
@@ -135,7 +136,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     fa::FwdParams prm;
     prm.lse = lse;
     prm.N = N;
-    prm.num_q_tiles = static_cast<int>(nq);
+    prm.num_q_blocks = static_cast<int>(nq);
     prm.scale = scale;
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     prm.timeout_ns = static_cast<unsigned long long>(timeout_s * 1e9);
