@@ -310,22 +310,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ====================================================== tensor-core issuer
         constexpr uint32_t idesc_s = instr_desc(BF16, kTileM, kBlockN, false);
         constexpr uint32_t idesc_pv = instr_desc(BF16, kTileM, D, true);
+        // Descriptor steps along K (16-byte units): Q and K advance 32 bytes per
+        // 16-element step inside a 128-byte swizzle row and jump to the next
+        // 64-column sub-tile after four; V advances 16 rows (2048 bytes).
+        constexpr uint32_t qk_step[8] = {0, 2, 4, 6, kSubBytes / 16, kSubBytes / 16 + 2,
+                                         kSubBytes / 16 + 4, kSubBytes / 16 + 6};
+        constexpr uint32_t qk_step4[4] = {0, 2, 4, 6};
+        constexpr uint32_t v_step[8] = {0, 128, 256, 384, 512, 640, 768, 896};
+        // stage s of a ring (and tile x of Q) is kTileBytes further on: its
+        // descriptor is the first one plus that offset in 16-byte units
+        constexpr uint64_t kTileStep = C::kTileBytes / 16;
+        const uint64_t q_desc0 = smem_desc(sQ(0), 16, 1024);
+        const uint64_t k_desc0 = smem_desc(sK(0), 16, 1024);
+        const uint64_t v_desc0 = smem_desc(sV(0), kSubBytes, 1024);
         // S_x = Q_x K_s^T into TMEM columns [128 x, 128 x + 128)
         auto issue_s = [&](int x, int s) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-                ptx::mma_ss_elect(tmem + x * 128, smem_desc(sQ(x) + off, 16, 1024),
-                                  smem_desc(sK(s) + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-            }
+            const uint64_t qd = q_desc0 + x * kTileStep, kd = k_desc0 + s * kTileStep;
+            if constexpr (D == 128)
+                ptx::mma_ss_group8(tmem + x * 128, qd, kd, idesc_s, 0u, qk_step, qk_step);
+            else
+                ptx::mma_ss_group4(tmem + x * 128, qd, kd, idesc_s, 0u, qk_step4, qk_step4);
         };
         // U_x (+)= P_x V_s, P_x read from TMEM: 128 keys = 8 K-steps of 16
         auto issue_pv = [&](int x, int s, bool acc) {
-#pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-                ptx::mma_ts_elect(tmem + kTmemU + x * 128, tmem + x * 128 + kk * 8,
-                                  smem_desc(sV(s) + kk * 2048, kSubBytes, 1024), idesc_pv,
-                                  (acc || kk > 0) ? 1u : 0u);
+            ptx::mma_ts_group8(tmem + kTmemU + x * 128, tmem + x * 128, v_desc0 + s * kTileStep,
+                               idesc_pv, acc ? 1u : 0u, v_step);
         };
         bool ok = wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
         if (ok) {
@@ -414,14 +423,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= limit) sv[c] = __float_as_uint(-INFINITY);
             }
-            // tile maximum of the raw scores
+            // tile maximum of the raw scores (eight chains of three-input max)
             float mx[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sv[u]);
 #pragma unroll
-            for (int c = 8; c < kBlockN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sv[c]));
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int c = 8; c + 16 <= kBlockN; c += 16)
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    mx[u] = ptx::fmax3(mx[u], __uint_as_float(sv[c + u]), __uint_as_float(sv[c + 8 + u]));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(sv[kBlockN - 8 + u]));
+            const float mt = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
+                                        fmaxf(mx[6], mx[7]));
             float alpha = 1.f;
             float m_new = m_ref;
             if (m_ref == -INFINITY) {

@@ -198,6 +198,106 @@ __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
         : "memory");
 }
 
+// One elected lane issues a group of tcgen05.mma kind::f16 instructions that
+// walk the K dimension: descriptor k of A and B is the base descriptor plus
+// a_step[k] / b_step[k] (16-byte units, added to the start-address field,
+// which cannot carry out for shared addresses below 256 KB).  The first
+// instruction overwrites D unless `accumulate`; the rest accumulate.
+// SS form: A and B from shared memory, 8 steps.
+__device__ __forceinline__ void mma_ss_group8(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                              uint32_t idesc, uint32_t accumulate,
+                                              const uint32_t (&a_step)[8],
+                                              const uint32_t (&b_step)[8]) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %12;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %13;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %14;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %8;\n\tadd.s64 b, %2, %15;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %16;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %10;\n\tadd.s64 b, %2, %17;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %18;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)a_step[1]),
+        "l"((uint64_t)a_step[2]), "l"((uint64_t)a_step[3]), "l"((uint64_t)a_step[4]),
+        "l"((uint64_t)a_step[5]), "l"((uint64_t)a_step[6]), "l"((uint64_t)a_step[7]),
+        "l"((uint64_t)b_step[1]), "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3]),
+        "l"((uint64_t)b_step[4]), "l"((uint64_t)b_step[5]), "l"((uint64_t)b_step[6]),
+        "l"((uint64_t)b_step[7])
+        : "memory");
+}
+
+// SS form, 4 steps.
+__device__ __forceinline__ void mma_ss_group4(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                              uint32_t idesc, uint32_t accumulate,
+                                              const uint32_t (&a_step)[4],
+                                              const uint32_t (&b_step)[4]) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 a, b;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
+        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %10;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)a_step[1]),
+        "l"((uint64_t)a_step[2]), "l"((uint64_t)a_step[3]), "l"((uint64_t)b_step[1]),
+        "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3])
+        : "memory");
+}
+
+// TS form (A from tensor memory), 8 steps: A advances by 8 columns (16
+// 16-bit elements) per step, B by b_step[k].
+__device__ __forceinline__ void mma_ts_group8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                              uint32_t idesc, uint32_t accumulate,
+                                              const uint32_t (&b_step)[8]) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)b_step[1]),
+        "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3]), "l"((uint64_t)b_step[4]),
+        "l"((uint64_t)b_step[5]), "l"((uint64_t)b_step[6]), "l"((uint64_t)b_step[7])
+        : "memory");
+}
+
+// Maximum of three values (sm_100+ three-input form).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
 // columns [taddr.col, +32) of lane (taddr.lane + t).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
