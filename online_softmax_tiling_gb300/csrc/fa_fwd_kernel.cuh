@@ -177,6 +177,29 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     }
 }
 
+// acc.x += lo, acc.y += hi of a packed 16-bit pair: each half is widened
+// exactly and added in fp32 (round to nearest) by one mixed-precision add.
+template <bool BF16>
+__device__ __forceinline__ void add_packed(float2& acc, uint32_t v) {
+    if constexpr (BF16)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc.x), "+f"(acc.y)
+            : "r"(v));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(acc.x), "+f"(acc.y)
+            : "r"(v));
+}
+
+// Weights are first computed against the current reference maximum; the tile
+// maximum is only taken when their fp32 sum exceeds this bound, which keeps
+// every weight finite and exact-range in the 16-bit type (all weights are
+// >= 0, so each is at most the sum).
+template <bool BF16>
+__host__ __device__ constexpr float weight_sum_limit() { return BF16 ? 4294967296.0f : 32768.0f; }
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -310,15 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ====================================================== tensor-core issuer
         constexpr uint32_t idesc_s = instr_desc(BF16, kTileM, kBlockN, false);
         constexpr uint32_t idesc_pv = instr_desc(BF16, kTileM, D, true);
-        // Descriptor steps along K (16-byte units): Q and K advance 32 bytes per
-        // 16-element step inside a 128-byte swizzle row and jump to the next
-        // 64-column sub-tile after four; V advances 16 rows (2048 bytes).
-        constexpr uint32_t qk_step[8] = {0, 2, 4, 6, kSubBytes / 16, kSubBytes / 16 + 2,
-                                         kSubBytes / 16 + 4, kSubBytes / 16 + 6};
-        constexpr uint32_t qk_step4[4] = {0, 2, 4, 6};
-        constexpr uint32_t v_step[8] = {0, 128, 256, 384, 512, 640, 768, 896};
         // stage s of a ring (and tile x of Q) is kTileBytes further on: its
-        // descriptor is the first one plus that offset in 16-byte units
+        // descriptor is the first one plus that offset in 16-byte units; the
+        // steps along K inside a group are built into the mma_*_k* helpers
         constexpr uint64_t kTileStep = C::kTileBytes / 16;
         const uint64_t q_desc0 = smem_desc(sQ(0), 16, 1024);
         const uint64_t k_desc0 = smem_desc(sK(0), 16, 1024);
@@ -327,14 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_s = [&](int x, int s) {
             const uint64_t qd = q_desc0 + x * kTileStep, kd = k_desc0 + s * kTileStep;
             if constexpr (D == 128)
-                ptx::mma_ss_group8(tmem + x * 128, qd, kd, idesc_s, 0u, qk_step, qk_step);
+                ptx::mma_ss_k128(tmem + x * 128, qd, kd, idesc_s, 0u);
             else
-                ptx::mma_ss_group4(tmem + x * 128, qd, kd, idesc_s, 0u, qk_step4, qk_step4);
+                ptx::mma_ss_k64(tmem + x * 128, qd, kd, idesc_s, 0u);
         };
         // U_x (+)= P_x V_s, P_x read from TMEM: 128 keys = 8 K-steps of 16
         auto issue_pv = [&](int x, int s, bool acc) {
-            ptx::mma_ts_group8(tmem + kTmemU + x * 128, tmem + x * 128, v_desc0 + s * kTileStep,
-                               idesc_pv, acc ? 1u : 0u, v_step);
+            ptx::mma_ts_k128(tmem + kTmemU + x * 128, tmem + x * 128, v_desc0 + s * kTileStep,
+                             idesc_pv, acc ? 1u : 0u);
         };
         bool ok = wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
         if (ok) {
@@ -394,18 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t u_addr = tmem + lane_off + kTmemU + x * 128;
         const float c2 = p.scale_log2;
         const float2 c2v = make_float2(c2, c2);
-        float m_ref = -INFINITY;              // reference maximum of the raw scores
-        float2 lsum = make_float2(0.f, 0.f);  // fp32 weights (for LSE), two partial sums
-        float2 lhat = make_float2(0.f, 0.f);  // 16-bit weights fed to P.V (for O)
-        bool aborted = false;
-
-        for (int j = 0; j < T; ++j) {
-            if (!wait_warp(bar_sf(x), j & 1, abort, tmo)) {
-                aborted = true;
-                break;
-            }
-            ptx::tc_fence_after_sync();
-            uint32_t sv[kBlockN];
+        // this row's 128 scores of the current tile, with keys >= N and, on the
+        // diagonal tile, keys in the future masked to -inf
+        auto load_scores = [&](uint32_t(&sv)[kBlockN], int j) {
 #pragma unroll
             for (int c = 0; c < kBlockN / 32; ++c)
                 ptx::tmem_ld_32x32b_x32(s_addr + c * 32,
@@ -413,8 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) ptx::reg_fence(sv[c]);
-
-            // mask keys >= N and, on the diagonal tile, keys in the future
             if (j == T - 1) {
                 const int kbase = j * kBlockN;
                 int limit = p.N - kbase;
@@ -423,58 +429,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= limit) sv[c] = __float_as_uint(-INFINITY);
             }
-            // tile maximum of the raw scores (eight chains of three-input max)
-            float mx[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(sv[u]);
-#pragma unroll
-            for (int c = 8; c + 16 <= kBlockN; c += 16)
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    mx[u] = ptx::fmax3(mx[u], __uint_as_float(sv[c + u]), __uint_as_float(sv[c + 8 + u]));
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(sv[kBlockN - 8 + u]));
-            const float mt = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]), ptx::fmax3(mx[3], mx[4], mx[5]),
-                                        fmaxf(mx[6], mx[7]));
-            float alpha = 1.f;
-            float m_new = m_ref;
-            if (m_ref == -INFINITY) {
-                m_new = mt;
-            } else if ((mt - m_ref) * c2 > kRescaleLog2) {
-                m_new = mt;
-                alpha = ptx::ex2_approx((m_ref - mt) * c2);
-            }
-            const float2 av = make_float2(alpha, alpha);
-            // a row with no valid key so far keeps all weights at zero
-            const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
+        };
+        // weights 2^(x c2 + neg_ref) of 2n scores, packed to 16 bits; the fp32
+        // weights are added to rs and the rounded ones (those fed to P.V) to rh
+        auto weights = [&](const uint32_t* sv, int n, float neg_ref, uint32_t* pk, float2 (&rs)[2],
+                           float2 (&rh)[2]) {
             const float2 nrv = make_float2(neg_ref, neg_ref);
-            // weights 2^(x c2 - m c2), their sums, and the packed 16-bit copy
-            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t pk[kBlockN / 2];
 #pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
+            for (int c = 0; c < n; ++c) {
                 const float2 e = __ffma2_rn(
                     make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2v, nrv);
                 const float2 pw = make_float2(ptx::ex2_approx(e.x), ptx::ex2_approx(e.y));
                 rs[c & 1] = __fadd2_rn(rs[c & 1], pw);
                 pk[c] = pack2<BF16>(pw.x, pw.y);
-                rh[c & 1] = __fadd2_rn(rh[c & 1], unpack2<BF16>(pk[c]));
+                add_packed<BF16>(rh[c & 1], pk[c]);
             }
-            lsum = __ffma2_rn(lsum, av, __fadd2_rn(rs[0], rs[1]));
-            lhat = __ffma2_rn(lhat, av, __fadd2_rn(rh[0], rh[1]));
+        };
+        // scores [32 c, 32 c + 32) of this row, masked like load_scores
+        auto load_chunk = [&](uint32_t(&sv)[32], int c, int j) {
+            ptx::tmem_ld_32x32b_x32(s_addr + c * 32, sv);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) ptx::reg_fence(sv[u]);
+            if (j == T - 1) {
+                const int kbase = j * kBlockN + c * 32;
+                int limit = p.N - kbase;
+                if (CAUSAL) limit = min(limit, row - kbase + 1);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    if (u >= limit) sv[u] = __float_as_uint(-INFINITY);
+            }
+        };
+        float m_ref = -INFINITY;              // reference maximum of the raw scores
+        float2 lsum = make_float2(0.f, 0.f);  // sum of the fp32 weights (for LSE) in .x
+        float2 lhat = make_float2(0.f, 0.f);  // sum of the 16-bit weights fed to P.V (for O) in .x
+        bool aborted = false;
+
+        for (int j = 0; j < T; ++j) {
+            if (!wait_warp(bar_sf(x), j & 1, abort, tmo)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            // common case: weights against the current reference, checked by
+            // their sum before they are written; the first tile (no reference
+            // yet) or a sum above the bound takes the tile maximum and
+            // recomputes from the scores still in TMEM (warp-uniform)
+            uint32_t pk[kBlockN / 2];
+            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            // (tcgen05.ld is warp-collective: every branch around it is uniform)
+            bool redo = (m_ref == -INFINITY);
+            if (!__any_sync(0xffffffffu, redo)) {
+                uint32_t sv[kBlockN];
+                load_scores(sv, j);
+                weights(sv, kBlockN / 2, -m_ref * c2, pk, rs, rh);
+                redo = rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
+            }
+            float alpha = 1.f;
+            float m_new = m_ref;
+            if (__any_sync(0xffffffffu, redo)) {
+                float mt = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < kBlockN / 32; ++c) {
+                    uint32_t sv[32];
+                    load_chunk(sv, c, j);
+                    float mx[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
+#pragma unroll
+                    for (int u = 4; u + 8 <= 32; u += 8)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
+                                               __uint_as_float(sv[u + 4 + w]));
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
+                    mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                }
+                // lanes whose weights were in range keep their reference
+                if (redo) {
+                    m_new = fmaxf(mt, m_ref);
+                    if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                }
+                // a row with no valid key so far keeps all weights at zero
+                const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
+                rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < kBlockN / 32; ++c) {
+                    uint32_t sv[32];
+                    load_chunk(sv, c, j);
+                    weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
+                }
+            }
+            const float2 av = make_float2(alpha, alpha);
+            const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
+            lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
+            lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
             ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
             ptx::tmem_st_32x32b_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
             // U_x already holds P(j-1) V: S_x(j) was issued after that product.
             // Rescale it by alpha when the reference maximum moved (warp-uniform).
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+#pragma unroll 1
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t ov[16];
+                    ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; u += 2) {
+                    for (int u = 0; u < 16; u += 2) {
                         ptx::reg_fence(ov[u]);
                         ptx::reg_fence(ov[u + 1]);
                         const float2 r = __fmul2_rn(
@@ -482,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ov[u] = __float_as_uint(r.x);
                         ov[u + 1] = __float_as_uint(r.y);
                     }
-                    ptx::tmem_st_32x32b_x32(u_addr + c * 32, ov);
+                    ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
                 }
             }
             ptx::tmem_wait_st();

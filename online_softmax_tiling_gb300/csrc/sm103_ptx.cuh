@@ -199,95 +199,85 @@ __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
 }
 
 // One elected lane issues a group of tcgen05.mma kind::f16 instructions that
-// walk the K dimension: descriptor k of A and B is the base descriptor plus
-// a_step[k] / b_step[k] (16-byte units, added to the start-address field,
-// which cannot carry out for shared addresses below 256 KB).  The first
-// instruction overwrites D unless `accumulate`; the rest accumulate.
-// SS form: A and B from shared memory, 8 steps.
-__device__ __forceinline__ void mma_ss_group8(uint32_t d_tmem, uint64_t a0, uint64_t b0,
-                                              uint32_t idesc, uint32_t accumulate,
-                                              const uint32_t (&a_step)[8],
-                                              const uint32_t (&b_step)[8]) {
+// walk the K dimension of operands laid out by TMA with 128-byte swizzle in
+// 128-row x 64-column sub-tiles of 16 KiB.  Descriptor k is the base
+// descriptor plus a constant (16-byte units, added to the start-address
+// field, which cannot carry out for shared addresses below 256 KB):
+//   K-major (Q, K): +32 bytes per 16-element step inside a swizzle row, +16 KiB
+//                   to the next sub-tile after four steps;
+//   MN-major (V):   +16 rows = 2048 bytes per step;
+//   A in TMEM (P):  +8 columns (16 16-bit elements) per step.
+// The first instruction overwrites D unless `accumulate`; the rest accumulate.
+// SS form, K = 128 (d = 128): 8 steps.
+__device__ __forceinline__ void mma_ss_k128(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 a, b;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\t"
         "setp.eq.b32 p1, %4, %4;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
-        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %12;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %13;\n\t"
+        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %14;\n\t"
+        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %8;\n\tadd.s64 b, %2, %15;\n\t"
+        "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %16;\n\t"
+        "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %10;\n\tadd.s64 b, %2, %17;\n\t"
+        "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %18;\n\t"
+        "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)a_step[1]),
-        "l"((uint64_t)a_step[2]), "l"((uint64_t)a_step[3]), "l"((uint64_t)a_step[4]),
-        "l"((uint64_t)a_step[5]), "l"((uint64_t)a_step[6]), "l"((uint64_t)a_step[7]),
-        "l"((uint64_t)b_step[1]), "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3]),
-        "l"((uint64_t)b_step[4]), "l"((uint64_t)b_step[5]), "l"((uint64_t)b_step[6]),
-        "l"((uint64_t)b_step[7])
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// SS form, 4 steps.
-__device__ __forceinline__ void mma_ss_group4(uint32_t d_tmem, uint64_t a0, uint64_t b0,
-                                              uint32_t idesc, uint32_t accumulate,
-                                              const uint32_t (&a_step)[4],
-                                              const uint32_t (&b_step)[4]) {
+// SS form, K = 64 (d = 64): 4 steps.
+__device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 a, b;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\t"
         "setp.eq.b32 p1, %4, %4;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
-        "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %8;\n\t"
+        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %6;\n\tadd.s64 b, %2, %9;\n\t"
+        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t"
-        "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %10;\n\t"
+        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)a_step[1]),
-        "l"((uint64_t)a_step[2]), "l"((uint64_t)a_step[3]), "l"((uint64_t)b_step[1]),
-        "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3])
+        "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// TS form (A from tensor memory), 8 steps: A advances by 8 columns (16
-// 16-bit elements) per step, B by b_step[k].
-__device__ __forceinline__ void mma_ts_group8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
-                                              uint32_t idesc, uint32_t accumulate,
-                                              const uint32_t (&b_step)[8]) {
+// TS form (A = P from tensor memory, B = V MN-major), K = 128 keys: 8 steps.
+__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p0, %4, 0;\n\t"
         "setp.eq.b32 p1, %4, %4;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
-        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, %5;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, %6;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, %7;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, %8;\n\t"
+        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, %9;\n\t"
+        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, %10;\n\t"
+        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, %11;\n\t"
+        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate), "l"((uint64_t)b_step[1]),
-        "l"((uint64_t)b_step[2]), "l"((uint64_t)b_step[3]), "l"((uint64_t)b_step[4]),
-        "l"((uint64_t)b_step[5]), "l"((uint64_t)b_step[6]), "l"((uint64_t)b_step[7])
+        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -325,6 +315,26 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
         : "memory");
 }
 

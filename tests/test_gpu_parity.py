@@ -100,6 +100,27 @@ def test_wide_score_range_rescales():
         parity.assert_within(st, f"wide causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", [synth.FP16, synth.BF16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_growing_keys_move_the_reference(dtype, causal):
+    """Key magnitudes that grow tile by tile: later tiles' weights overflow the
+    bound against the stale reference, so the maximum is re-taken, U is
+    rescaled and the weights recomputed."""
+    B, H, N, d = 1, 2, 1000, 128
+    q = synth.tensor_bits(601, (B, H, N, d), dtype)
+    kf = synth.bits_to_float(synth.tensor_bits(602, (B, H, N, d), dtype), dtype).astype(np.float64)
+    growth = 6.0 if dtype == synth.FP16 else 40.0
+    kf *= (1.0 + growth * (np.arange(N) // 128) / 7.0)[None, None, :, None]
+    k = synth.round_to_bits(kf, dtype)
+    v = synth.tensor_bits(603, (B, H, N, d), dtype)
+    scale = 1.0 / math.sqrt(d)
+    o, lse, _ = parity.run_gpu(q, k, v, dtype, scale, causal)
+    rows = np.arange(B * H * N, dtype=np.int64)
+    o_ref, lse_ref, spread = parity.oracle_rows(q, k, v, dtype, scale, causal, rows)
+    st = parity.compare(o.reshape(-1, d), lse.reshape(-1), o_ref, lse_ref, spread, dtype)
+    parity.assert_within(st, f"growing keys dtype={dtype} causal={causal}")
+
+
 _INPUTS = {}
 
 
