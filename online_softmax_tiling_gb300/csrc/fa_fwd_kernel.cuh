@@ -27,10 +27,14 @@
 //     tensor core overlap.  Because S_X(j+1) is issued after PV_X(j), its
 //     completion also means U_X holds P_X(j) V_j: the softmax warps may
 //     rescale U_X right away, without another wait.
-//   * the running maximum only moves when it grows by more than 2^8 in
-//     weight units; until then the weights stay <= 256 and l, U keep the old
-//     reference, which is exact because l, U and LSE all refer to the same m.
-//     U is rescaled in TMEM only on those rare steps.
+//   * weights are computed against the running reference maximum m of the
+//     previous tiles, without taking the new tile's maximum first; their fp32
+//     sum bounds every weight (all are >= 0), so while it stays below a bound
+//     that keeps each weight inside the 16-bit type, l, U and the weights keep
+//     the old reference, which is exact because l, U and LSE all refer to the
+//     same m.  Only the first tile of a row, or a tile whose weights would
+//     pass the bound, takes the tile maximum, moves m, rescales U in TMEM and
+//     recomputes the weights from the scores still in TMEM.
 //   * O is normalised by the sum of the 16-bit weights actually fed to P.V,
 //     so it is an exact convex combination of those weights; LSE uses the sum
 //     of the fp32 weights.
@@ -59,7 +63,6 @@ constexpr int kMmaWarp = 9;
 constexpr int kSubBytes = 128 * 128;  // one 128-row x 64-column 16-bit swizzle sub-tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemU = 256;      // U_A at 256, U_B at 384
-constexpr float kRescaleLog2 = 8.0f;  // move m only when weights would exceed 2^8
 
 // Device status word (FA_OK / FA_ERR_TIMEOUT); read and cleared by the host.
 __device__ unsigned int g_fa_status;
