@@ -21,6 +21,8 @@
 #ifndef FA_GB300_FA_H
 #define FA_GB300_FA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -68,6 +70,41 @@ extern "C" {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, int dtype,
            void* stream);
+
+/*
+ * Split-KV ("CUDA 算子工程" ch. 14, section 14.7.1): when B*H*ceil(N/256) query
+ * blocks cannot fill the GPU, the key tiles of every block are divided into
+ * num_splits contiguous ranges processed by separate CTAs; each writes a
+ * partial O (fp32, normalised by its own weights) and partial log-sum-exps to
+ * a caller-provided workspace, and a second kernel merges them:
+ *   LSE = ln sum_s e^{LSE_s},  O = sum_s w_s O_s / sum_s w_s,
+ * w_s being range s's sum of the 16-bit weights fed to P.V on a common scale.
+ * The result matches fa_fwd within rounding.
+ */
+#define FA_MAX_SPLITS 32
+
+/* Split count the library would choose for this shape on the current device
+ * (about two waves of CTAs, at least four key tiles per split); 1 means that
+ * fa_fwd already fills the GPU. */
+int fa_splitkv_num_splits(int B, int H, int N, int d, int causal);
+
+/* Workspace bytes fa_fwd_splitkv needs for num_splits >= 2 (0 otherwise). */
+size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/*
+ * fa_fwd_splitkv - fa_fwd computed in num_splits key ranges plus a merge.
+ * Arguments as fa_fwd, plus:
+ * num_splits      : 1 = plain fa_fwd (workspace unused), 2..FA_MAX_SPLITS =
+ *                   that many ranges, 0 = fa_splitkv_num_splits().
+ * workspace       : device memory owned by the caller, 256-byte aligned, at
+ *                   least fa_splitkv_workspace_size() bytes; overwritten; must
+ *                   not be shared by calls that may run at the same time.
+ * workspace_bytes : its size (FA_ERR_INVALID_ARG if too small).
+ * Both kernels are enqueued on `stream`; the library allocates nothing.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal, int dtype,
+                   int num_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_check_device_status - synchronise `stream`, then return and clear the

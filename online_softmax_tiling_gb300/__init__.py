@@ -22,7 +22,9 @@ FA_FP16, FA_BF16 = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
-EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug")
+EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug",
+           "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv")
+FA_MAX_SPLITS = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +58,13 @@ def library() -> ctypes.CDLL:
             lib.fa_status_string.restype = ctypes.c_char_p
             lib.fa_version.argtypes = []
             lib.fa_version.restype = i
+            lib.fa_splitkv_num_splits.argtypes = [i, i, i, i, i]
+            lib.fa_splitkv_num_splits.restype = i
+            lib.fa_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+            lib.fa_splitkv_workspace_size.restype = ctypes.c_size_t
+            lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, i, i,
+                                           vp, ctypes.c_size_t, vp]
+            lib.fa_fwd_splitkv.restype = i
             _lib = lib
         return _lib
 
@@ -71,6 +80,22 @@ def fa_fwd_debug(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, faul
     return library().fa_fwd_debug(q, k, v, o, lse, int(B), int(H), int(N), int(d), float(scale),
                                   int(causal), int(dtype), stream, int(fault_mode),
                                   float(timeout_s))
+
+
+def fa_splitkv_num_splits(B, H, N, d, causal) -> int:
+    return library().fa_splitkv_num_splits(int(B), int(H), int(N), int(d), int(causal))
+
+
+def fa_splitkv_workspace_size(B, H, N, d, num_splits) -> int:
+    return library().fa_splitkv_workspace_size(int(B), int(H), int(N), int(d), int(num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits, workspace,
+                   workspace_bytes, stream) -> int:
+    """Raw C call of the split-KV entry point (addresses as integers or None)."""
+    return library().fa_fwd_splitkv(q, k, v, o, lse, int(B), int(H), int(N), int(d),
+                                    float(scale), int(causal), int(dtype), int(num_splits),
+                                    workspace, int(workspace_bytes), stream)
 
 
 def fa_check_device_status(stream=None) -> int:
@@ -98,12 +123,15 @@ def _dtype_code(t) -> int:
 
 
 def attention_forward(q, k, v, scale: float | None = None, causal: bool = False, out=None,
-                      lse=None, stream=None):
+                      lse=None, stream=None, num_splits: int = 1):
     """O, LSE for contiguous CUDA tensors q, k, v of shape [B, H, N, d].
 
     scale defaults to 1/sqrt(d).  Outputs are allocated with torch unless
-    given.  Raises FaError on any non-OK status.  Asynchronous on `stream`
-    (default: torch's current stream).
+    given.  num_splits: 1 = one fused launch (fa_fwd); 0 = let the library
+    choose a split-KV count for shapes that cannot fill the GPU; >= 2 = that
+    many key ranges (fa_fwd_splitkv, with a workspace allocated by torch).
+    Raises FaError on any non-OK status.  Asynchronous on `stream` (default:
+    torch's current stream).
     """
     import torch
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
@@ -121,8 +149,17 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
-    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
-                N, d, scale, causal, _dtype_code(q), handle)
+    if num_splits == 0:
+        num_splits = fa_splitkv_num_splits(B, H, N, d, causal)
+    if num_splits == 1:
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                    N, d, scale, causal, _dtype_code(q), handle)
+    else:
+        nbytes = fa_splitkv_workspace_size(B, H, N, d, num_splits)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr(), B, H, N, d, scale, causal, _dtype_code(q), num_splits,
+                            ws.data_ptr(), nbytes, handle)
     if st != FA_OK:
         raise FaError(st)
     return out, lse

@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -58,39 +59,46 @@ bool encode_qkvo(CUtensorMap* map, const void* ptr, int dtype, int64_t BH, int64
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, fa::FwdParams);
-
-template <int D, bool BF16, bool CAUSAL>
-KernelFn kernel_of() {
-    return reinterpret_cast<KernelFn>(&fa::fa_fwd_kernel<D, BF16, CAUSAL>);
-}
-
 struct KernelEntry {
     const void* fn;
     int smem;
 };
 
-KernelEntry select_kernel(int d, int dtype, bool causal) {
-#define FA_ENTRY(D, BF, CA) \
-    KernelEntry { reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF, CA>), fa::Cfg<D>::kSmemBytes }
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+KernelEntry entry() {
+    return KernelEntry{reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>),
+                       fa::Cfg<D>::kSmemBytes};
+}
+
+template <int D, bool BF16>
+KernelEntry select_d_dtype(bool causal, bool split) {
+    if (causal) return split ? entry<D, BF16, true, true>() : entry<D, BF16, true, false>();
+    return split ? entry<D, BF16, false, true>() : entry<D, BF16, false, false>();
+}
+
+KernelEntry select_kernel(int d, int dtype, bool causal, bool split) {
     const bool bf = dtype == FA_BF16;
-    if (d == 64) {
-        if (bf) return causal ? FA_ENTRY(64, true, true) : FA_ENTRY(64, true, false);
-        return causal ? FA_ENTRY(64, false, true) : FA_ENTRY(64, false, false);
-    }
-    if (bf) return causal ? FA_ENTRY(128, true, true) : FA_ENTRY(128, true, false);
-    return causal ? FA_ENTRY(128, false, true) : FA_ENTRY(128, false, false);
-#undef FA_ENTRY
+    if (d == 64) return bf ? select_d_dtype<64, true>(causal, split) : select_d_dtype<64, false>(causal, split);
+    return bf ? select_d_dtype<128, true>(causal, split) : select_d_dtype<128, false>(causal, split);
+}
+
+const void* select_merge(int d, int dtype) {
+    const bool bf = dtype == FA_BF16;
+    if (d == 64)
+        return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<64, true>)
+                  : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<64, false>);
+    return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<128, true>)
+              : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<128, false>);
 }
 
 // Opt each kernel into its dynamic shared memory once per device.
 bool ensure_smem_attr(const void* fn, int smem, int device) {
     static std::mutex mu;
-    static std::atomic<uint64_t> done_mask[8][64];  // [kernel slot][device / 64 word]
-    static const void* slots[8] = {};
+    static std::atomic<uint64_t> done_mask[16][64];  // [kernel slot][device / 64 word]
+    static const void* slots[16] = {};
     std::lock_guard<std::mutex> lock(mu);
     int slot = -1;
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
         if (slots[i] == fn) { slot = i; break; }
         if (slots[i] == nullptr) { slots[i] = fn; slot = i; break; }
     }
@@ -103,9 +111,19 @@ bool ensure_smem_attr(const void* fn, int smem, int device) {
     return true;
 }
 
+// Workspace layout of split-KV: o_part [S][BH][N][d] fp32, then (256-byte
+// aligned) lse_part [2][S][BH][N] fp32.
+size_t split_o_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
+    return (static_cast<size_t>(S * BH * N * d) * 4 + 255) & ~static_cast<size_t>(255);
+}
+size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
+    return split_o_bytes(S, BH, N, d) + static_cast<size_t>(2 * S * BH * N) * 4;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int N, int d, float scale, int causal, int dtype, void* stream, int fault_mode,
-             double timeout_s) {
+             double timeout_s, int num_splits = 1, void* workspace = nullptr,
+             size_t workspace_bytes = 0) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
@@ -122,6 +140,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
         misaligned(lse, 4))
         return FA_ERR_MISALIGNED;
+    const bool split = num_splits > 1;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    if (split) {
+        if (!workspace) return FA_ERR_INVALID_ARG;
+        if (misaligned(workspace, 256)) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < split_workspace_bytes(num_splits, BH, N, d)) return FA_ERR_INVALID_ARG;
+        if (BH * nq * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
+    }
 
     CUtensorMap tq, tk, tv, to;
     if (!encode_qkvo(&tq, q, dtype, BH, N, d) || !encode_qkvo(&tk, k, dtype, BH, N, d) ||
@@ -130,7 +156,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
-    const KernelEntry ke = select_kernel(d, dtype, causal != 0);
+    const KernelEntry ke = select_kernel(d, dtype, causal != 0, split);
     if (!ensure_smem_attr(ke.fn, ke.smem, device)) return FA_ERR_CUDA;
 
     fa::FwdParams prm;
@@ -141,13 +167,29 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     prm.timeout_ns = static_cast<unsigned long long>(timeout_s * 1e9);
     prm.fault_mode = fault_mode;
+    prm.num_splits = num_splits;
+    prm.BH = static_cast<int>(BH);
+    prm.o_part = split ? static_cast<float*>(workspace) : nullptr;
+    prm.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    split_o_bytes(num_splits, BH, N, d))
+                         : nullptr;
 
     void* args[] = {&tq, &tk, &tv, &to, &prm};
-    const dim3 grid(static_cast<unsigned>(BH * nq));
+    const dim3 grid(static_cast<unsigned>(BH * nq * num_splits));
     const dim3 block(fa::kThreads);
-    if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem),
-                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem), st) != cudaSuccess)
         return FA_ERR_CUDA;
+    if (split) {
+        const long long rows = static_cast<long long>(BH) * N;
+        const float* op = prm.o_part;
+        const float* lp = prm.lse_part;
+        void* margs[] = {const_cast<float**>(&op), const_cast<float**>(&lp), &o, &lse,
+                         &num_splits, const_cast<long long*>(&rows)};
+        const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));
+        if (cudaLaunchKernel(select_merge(d, dtype), mgrid, dim3(256), margs, 0, st) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
     return FA_OK;
 }
 
@@ -165,6 +207,35 @@ int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* ls
                  double timeout_s) {
     return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, fault_mode,
                     timeout_s);
+}
+
+int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
+    (void)causal;
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 1;
+    int device = 0, sms = 148;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        sms = 148;
+    const int64_t ctas = static_cast<int64_t>(B) * H * ((N + fa::kBlockM - 1) / fa::kBlockM);
+    if (ctas >= sms) return 1;
+    const int64_t nkv = (static_cast<int64_t>(N) + fa::kBlockN - 1) / fa::kBlockN;
+    int64_t s = (2 * static_cast<int64_t>(sms) + ctas - 1) / ctas;  // about two waves
+    s = std::min<int64_t>(s, std::max<int64_t>(1, nkv / 4));      // >= 4 key tiles per split
+    s = std::min<int64_t>(s, FA_MAX_SPLITS);
+    return static_cast<int>(std::max<int64_t>(1, s));
+}
+
+size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || num_splits < 2) return 0;
+    return split_workspace_bytes(num_splits, static_cast<int64_t>(B) * H, N, d);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int dtype, int num_splits,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_splits == 0) num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0, num_splits,
+                    workspace, workspace_bytes);
 }
 
 int fa_check_device_status(void* stream) {

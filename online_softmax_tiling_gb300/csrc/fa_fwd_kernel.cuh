@@ -71,6 +71,13 @@ struct FwdParams {
     float* lse;
     int N;
     int num_q_blocks;  // ceil(N / 256)
+    // split-KV only: key tiles of each query block are divided into
+    // num_splits contiguous ranges; each CTA writes a partial result
+    int num_splits;
+    int BH;
+    float* o_part;    // [num_splits][BH][N][d] fp32, O of the range (normalised by its lhat)
+    float* lse_part;  // [2][num_splits][BH][N] fp32: LSE of the range, and its log-sum of
+                      // the rounded weights (the weight of its O in the merge)
     float scale;       // s
     float scale_log2;  // s * log2(e): exp(s x) = 2^(x * scale_log2)
     unsigned long long timeout_ns;
@@ -203,7 +210,7 @@ __device__ __forceinline__ void add_packed(float2& acc, uint32_t v) {
 template <bool BF16>
 __host__ __device__ constexpr float weight_sum_limit() { return BF16 ? 4294967296.0f : 32768.0f; }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -225,13 +232,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- which rows: consecutive CTAs share a head, so its K/V stay in L2;
     // with the causal mask the longest query blocks of each head start first.
-    const int bh = blockIdx.x / p.num_q_blocks;
-    int qb = blockIdx.x % p.num_q_blocks;
+    const int split = SPLIT ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
+    const int blk = SPLIT ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
+    const int bh = blk / p.num_q_blocks;
+    int qb = blk % p.num_q_blocks;
     if (CAUSAL) qb = p.num_q_blocks - 1 - qb;
     const int nkv = (p.N + kBlockN - 1) / kBlockN;
-    // key tiles visited by query tile A (rows qb*256 + [0,128)) and B ([128,256))
+    // key tiles visible to query tile A (rows qb*256 + [0,128)) and B ([128,256))
     const int T_A = CAUSAL ? min(2 * qb + 1, nkv) : nkv;
     const int T_B = CAUSAL ? min(2 * qb + 2, nkv) : nkv;
+    // this CTA visits key tiles k0 .. k0 + n_x - 1 for tile x (all of them
+    // unless split-KV divides the range of the block into num_splits parts)
+    int k0 = 0, nA = T_A, nB = T_B;
+    if constexpr (SPLIT) {
+        const int chunk = (T_B + p.num_splits - 1) / p.num_splits;
+        k0 = split * chunk;
+        const int k1 = min(k0 + chunk, T_B);
+        nB = max(0, k1 - k0);
+        nA = max(0, min(k1, T_A) - k0);
+        if (nB == 0) {  // empty range: its partials carry no weight
+            const int row = qb * kBlockM + static_cast<int>(threadIdx.x);
+            if (threadIdx.x < kBlockM && row < p.N) {
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.N + row;
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.N;
+                p.lse_part[i] = -INFINITY;
+                p.lse_part[plane + i] = -INFINITY;
+            }
+            return;
+        }
+    }
 
     const uint32_t bar_q = ptx::smem_addr(&ctl->q_full);
     auto bar_kf = [&](int s) { return ptx::smem_addr(&ctl->k_full[s]); };
@@ -298,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tma_load_3d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
                                      qb * kBlockM + x * kTileM, bh);
         }
-        for (int j = 0; j <= T_B; ++j) {
-            if (j < T_B) {
+        for (int j = 0; j <= nB; ++j) {
+            if (j < nB) {
                 const int s = j % NK;
                 if (j >= NK && !wait_warp(bar_ke(s), ((j / NK) - 1) & 1, abort, tmo)) break;
                 const bool skip = (p.fault_mode == 1 && j == 0);
@@ -308,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::kSub; ++c)
                         ptx::tma_load_3d(sK(s) + c * kSubBytes, &tm_k, bar_kf(s), 64 * c,
-                                         j * kBlockN, bh);
+                                         (k0 + j) * kBlockN, bh);
                 }
                 if (!skip) ++issued_k[s];
             }
@@ -321,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < C::kSub; ++c)
                         ptx::tma_load_3d(sV(s) + c * kSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                         jv * kBlockN, bh);
+                                         (k0 + jv) * kBlockN, bh);
                 }
                 ++issued_v[s];
             }
@@ -359,24 +388,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
         if (ok) {
             ptx::tc_fence_after_sync();
-            issue_s(0, 0);
-            ptx::tc_commit_elect(bar_sf(0));
+            if (nA > 0) {
+                issue_s(0, 0);
+                ptx::tc_commit_elect(bar_sf(0));
+            }
             issue_s(1, 0);
             ptx::tc_commit_elect(bar_sf(1));
             ptx::tc_commit_elect(bar_ke(0));
             __syncwarp();
         }
-        for (int j = 0; ok && j < T_B; ++j) {
+        for (int j = 0; ok && j < nB; ++j) {
             const int sv = j % NV;
             const int sk = (j + 1) % NK;
             bool k_ready = false;
             if (!(ok = wait_warp(bar_vf(sv), (j / NV) & 1, abort, tmo))) break;
-            if (j < T_A) {
+            if (j < nA) {
                 if (!(ok = wait_warp(bar_pf(0), j & 1, abort, tmo))) break;
                 ptx::tc_fence_after_sync();
                 issue_pv(0, sv, j > 0);
                 ptx::tc_commit_elect(bar_o(0));
-                if (j + 1 < T_A) {
+                if (j + 1 < nA) {
                     if (!(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
                     k_ready = true;
                     ptx::tc_fence_after_sync();
@@ -389,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             issue_pv(1, sv, j > 0);
             ptx::tc_commit_elect(bar_o(1));
-            if (j + 1 < T_B) {
+            if (j + 1 < nB) {
                 if (!k_ready && !(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
                 ptx::tc_fence_after_sync();
                 issue_s(1, sk);
@@ -408,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = warp >> 2;                          // 0: tile A, 1: tile B
         const int t = threadIdx.x & 127;                  // row in the tile = TMEM lane
         const int row = qb * kBlockM + x * kTileM + t;    // query index in the head
-        const int T = x == 0 ? T_A : T_B;
+        const int T = x == 0 ? nA : nB;          // key tiles this CTA visits for the tile
+        const int T_all = x == 0 ? T_A : T_B;    // key tiles visible to the tile
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + x * 128;
         const uint32_t u_addr = tmem + lane_off + kTmemU + x * 128;
@@ -424,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) ptx::reg_fence(sv[c]);
-            if (j == T - 1) {
-                const int kbase = j * kBlockN;
+            if (k0 + j == T_all - 1) {
+                const int kbase = (k0 + j) * kBlockN;
                 int limit = p.N - kbase;
                 if (CAUSAL) limit = min(limit, row - kbase + 1);
 #pragma unroll
@@ -454,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int u = 0; u < 32; ++u) ptx::reg_fence(sv[u]);
-            if (j == T - 1) {
-                const int kbase = j * kBlockN + c * 32;
+            if (k0 + j == T_all - 1) {
+                const int kbase = (k0 + j) * kBlockN + c * 32;
                 int limit = p.N - kbase;
                 if (CAUSAL) limit = min(limit, row - kbase + 1);
 #pragma unroll
@@ -558,10 +590,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ---- epilogue: O = U / lhat -> 16-bit -> swizzled smem -> TMA store
-        if (!aborted) aborted = !wait_warp(bar_o(x), (T - 1) & 1, abort, tmo);
+        if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (T - 1) & 1, abort, tmo);
         const float l_all = lsum.x + lsum.y;
         const float lhat_all = lhat.x + lhat.y;
-        if (!aborted) {
+        if constexpr (SPLIT) {
+            // partial result of this key range: O normalised by its own lhat
+            // (fp32) and the two log-sums that weight it in the merge
+            // (warp-uniform branches around the collective tcgen05.ld)
+            if (!aborted) {
+                const bool mine = row < p.N && !*abort;
+                const bool any = T > 0 && l_all > 0.f;
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.N + (mine ? row : 0);
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.N;
+                if (mine) {
+                    p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
+                    p.lse_part[plane + i] = any ? m_ref * p.scale + logf(lhat_all) : -INFINITY;
+                }
+                if (T > 0) {
+                    ptx::tc_fence_after_sync();
+                    const float inv = any ? 1.f / lhat_all : 0.f;
+                    float4* dst = reinterpret_cast<float4*>(p.o_part + i * D);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4) {
+                            ptx::reg_fence(ov[u]);
+                            ptx::reg_fence(ov[u + 1]);
+                            ptx::reg_fence(ov[u + 2]);
+                            ptx::reg_fence(ov[u + 3]);
+                            if (mine)
+                                dst[c * 8 + u / 4] = make_float4(
+                                    __uint_as_float(ov[u]) * inv, __uint_as_float(ov[u + 1]) * inv,
+                                    __uint_as_float(ov[u + 2]) * inv, __uint_as_float(ov[u + 3]) * inv);
+                        }
+                    }
+                }
+            }
+        } else if (!aborted) {
             ptx::tc_fence_after_sync();
             const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
             const float2 iv = make_float2(inv, inv);
@@ -596,14 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::fence_proxy_async_smem();
         }
         ptx::named_barrier_sync(1 + x, kTileM);
-        if (t == 0 && !*abort) {
+        if (!SPLIT && t == 0 && !*abort) {
 #pragma unroll
             for (int c = 0; c < C::kSub; ++c)
                 ptx::tma_store_3d(&tm_o, sQ(x) + c * kSubBytes, 64 * c, qb * kBlockM + x * kTileM, bh);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_read0();
         }
-        if (!aborted && !*abort && row < p.N) {
+        if (!SPLIT && !aborted && !*abort && row < p.N) {
             const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
             p.lse[static_cast<size_t>(bh) * p.N + row] = lse;
         }
@@ -614,6 +682,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- split-KV merge ("CUDA 算子工程" 14.7.1: every split writes a partial O
+// and LSE, merged afterwards).  Per query row: LSE = ln sum_s e^{LSE_s}, and
+// O = sum_s w_s O_s / sum_s w_s with w_s = e^{LSEhat_s - max}: O_s is
+// normalised by the sum of its rounded weights, so w_s is that sum on the
+// common scale, which keeps O an exact convex combination of every weight
+// fed to P.V.  A warp per row; each lane owns d/32 consecutive columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_split_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                          void* __restrict__ o, float* __restrict__ lse, int num_splits,
+                          long long rows) {
+    constexpr int kPer = D / 32;
+    const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const size_t plane = static_cast<size_t>(num_splits) * rows;
+    float mh = -INFINITY, ml = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) {
+        mh = fmaxf(mh, lse_part[plane + s * rows + r]);
+        ml = fmaxf(ml, lse_part[s * rows + r]);
+    }
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float wsum = 0.f, lsum = 0.f;
+    for (int s = 0; s < num_splits; ++s) {
+        const float lh = lse_part[plane + s * rows + r];
+        lsum += (ml == -INFINITY) ? 0.f : __expf(lse_part[s * rows + r] - ml);
+        if (lh == -INFINITY) continue;  // empty range: no weight, O_s not written
+        const float w = __expf(lh - mh);
+        wsum += w;
+        const float* src = o_part + (s * rows + r) * D + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; e += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(src + e);
+            acc[e] = fmaf(w, v.x, acc[e]);
+            acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint32_t packed[kPer / 2];
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) packed[e / 2] = pack2<BF16>(acc[e] * inv, acc[e + 1] * inv);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(o) + (r * D + lane * kPer) / 2;
+#pragma unroll
+    for (int e = 0; e < kPer / 2; ++e) dst[e] = packed[e];
+    if (lane == 0) lse[r] = (ml == -INFINITY) ? -INFINITY : ml + logf(lsum);
 }
 
 }  // namespace fa

@@ -76,8 +76,9 @@ def assert_within(stats: dict, label: str = ""):
     assert stats["lse_rel_max"] <= LSE_REL, f"{label}: {stats}"
 
 
-def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0):
-    """Run fa_fwd on uploaded inputs; returns (o_bits [B,H,N,d], lse [B,H,N], guards ok)."""
+def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0, num_splits: int = 1):
+    """Run fa_fwd (or fa_fwd_splitkv when num_splits != 1) on uploaded inputs;
+    returns (o_bits [B,H,N,d], lse [B,H,N], guards ok)."""
     import torch
     import online_softmax_tiling_gb300 as fa
     B, H, N, d = q_bits.shape
@@ -90,8 +91,16 @@ def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0):
     o = o_buf[guard:guard + n_o].view(B, H, N, d)
     lse = l_buf[guard:guard + B * H * N].view(B, H, N)
     stream = torch.cuda.current_stream()
-    st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                   B, H, N, d, scale, int(causal), dtype, stream.cuda_stream)
+    if num_splits == 1:
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, N, d, scale, int(causal), dtype, stream.cuda_stream)
+    else:
+        s_eff = num_splits or fa.fa_splitkv_num_splits(B, H, N, d, int(causal))
+        nbytes = max(fa.fa_splitkv_workspace_size(B, H, N, d, s_eff), 256)
+        ws = torch.full((nbytes + 2 * guard,), 0x7F, dtype=torch.uint8, device="cuda")
+        st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, scale, int(causal), dtype, num_splits,
+                               ws.data_ptr(), nbytes, stream.cuda_stream)
     assert st == fa.FA_OK, fa.fa_status_string(st)
     assert fa.fa_check_device_status(stream.cuda_stream) == fa.FA_OK
     guards_ok = True

@@ -80,3 +80,20 @@ def test_debug_entry_validates_its_controls(lib):
     assert fa.fa_fwd_debug(*base, 2, 1.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_debug(*base, 0, 0.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_debug(*base, 0, float("nan")) == fa.FA_ERR_INVALID_ARG
+
+
+def test_splitkv_workspace_size_and_validation(lib):
+    assert fa.fa_splitkv_workspace_size(1, 1, 128, 64, 1) == 0
+    need = fa.fa_splitkv_workspace_size(2, 3, 1000, 128, 4)
+    S, BH, N, d = 4, 6, 1000, 128
+    o_bytes = (4 * S * BH * N * d + 255) // 256 * 256       # fp32 partial O
+    assert need == o_bytes + 4 * 2 * S * BH * N              # two fp32 log-sums per row
+    base = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 2, 3, 1000, 128, 0.1, 0, fa.FA_BF16)
+    ws = 0x100000
+    assert fa.fa_fwd_splitkv(*base, 33, ws, need, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*base, -1, ws, need, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*base, 4, None, need, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv(*base, 4, ws + 16, need, None) == fa.FA_ERR_MISALIGNED
+    assert fa.fa_fwd_splitkv(*base, 4, ws, need - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert 1 <= fa.fa_splitkv_num_splits(1, 1, 4096, 64, 0) <= fa.FA_MAX_SPLITS
+    assert fa.fa_splitkv_num_splits(64, 64, 4096, 128, 0) == 1
