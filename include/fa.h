@@ -83,9 +83,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  */
 #define FA_MAX_SPLITS 32
 
-/* Split count the library would choose for this shape on the current device
- * (about two waves of CTAs, at least four key tiles per split); 1 means that
- * fa_fwd already fills the GPU. */
+/* Split count the library would choose for this shape on the current device:
+ * 1 (fa_fwd is better) unless the query blocks fill less than half of the SMs;
+ * then about one wave of CTAs, with at least four key tiles per range. */
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal);
 
 /* Workspace bytes fa_fwd_splitkv needs for num_splits >= 2 (0 otherwise). */

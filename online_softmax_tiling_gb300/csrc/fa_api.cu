@@ -216,11 +216,14 @@ int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         sms = 148;
+    // Splitting pays for its fp32 partials and merge only when most SMs would
+    // otherwise idle: split when the blocks fill less than half of them, into
+    // about one wave, keeping at least four key tiles per range.
     const int64_t ctas = static_cast<int64_t>(B) * H * ((N + fa::kBlockM - 1) / fa::kBlockM);
-    if (ctas >= sms) return 1;
+    if (2 * ctas > sms) return 1;
     const int64_t nkv = (static_cast<int64_t>(N) + fa::kBlockN - 1) / fa::kBlockN;
-    int64_t s = (2 * static_cast<int64_t>(sms) + ctas - 1) / ctas;  // about two waves
-    s = std::min<int64_t>(s, std::max<int64_t>(1, nkv / 4));      // >= 4 key tiles per split
+    int64_t s = (static_cast<int64_t>(sms) + ctas - 1) / ctas;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, nkv / 4));
     s = std::min<int64_t>(s, FA_MAX_SPLITS);
     return static_cast<int>(std::max<int64_t>(1, s));
 }
