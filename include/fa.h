@@ -107,6 +107,29 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int num_splits, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_fwd_splitkv_noalloc - fa_fwd_splitkv for callers that cannot allocate
+ * device memory (no counterpart on the pages: the pages do not discuss who
+ * allocates the split-KV partials).  Some callers cannot call cudaMalloc: a
+ * plugin whose host framework owns all device memory, or a latency-critical
+ * path that cannot take cudaMalloc's implicit synchronisation.  This entry
+ * point keeps the partials in a fixed array of FA_NOALLOC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until exit; it
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments as fa_fwd_splitkv without the workspace.  Returns
+ * FA_ERR_UNSUPPORTED when fa_splitkv_workspace_size() of the request is above
+ * FA_NOALLOC_SCRATCH_BYTES (use fa_fwd_splitkv with a workspace instead).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and its contents
+ * persist from call to call; calls that may overlap on the GPU race, so order
+ * them (one stream, or events).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal, int dtype,
+                           int num_splits, void* stream);
+
+/*
  * fa_check_device_status - synchronise `stream`, then return and clear the
  * device-side status word: FA_OK, FA_ERR_TIMEOUT (some CTA's bounded wait
  * expired and that CTA left its outputs unwritten), or FA_ERR_CUDA if the

@@ -23,7 +23,9 @@ FA_FP16, FA_BF16 = 0, 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
 EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug",
-           "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv")
+           "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv",
+           "fa_fwd_splitkv_noalloc")
+FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 FA_MAX_SPLITS = 32
 
 _lock = threading.Lock()
@@ -65,6 +67,9 @@ def library() -> ctypes.CDLL:
             lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, i, i,
                                            vp, ctypes.c_size_t, vp]
             lib.fa_fwd_splitkv.restype = i
+            lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float,
+                                                   i, i, i, vp]
+            lib.fa_fwd_splitkv_noalloc.restype = i
             _lib = lib
         return _lib
 
@@ -96,6 +101,15 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits
     return library().fa_fwd_splitkv(q, k, v, o, lse, int(B), int(H), int(N), int(d),
                                     float(scale), int(causal), int(dtype), int(num_splits),
                                     workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, num_splits,
+                           stream) -> int:
+    """Split-KV with the partials in the library's fixed scratch array, for
+    callers that cannot allocate device memory (see include/fa.h)."""
+    return library().fa_fwd_splitkv_noalloc(q, k, v, o, lse, int(B), int(H), int(N), int(d),
+                                            float(scale), int(causal), int(dtype),
+                                            int(num_splits), stream)
 
 
 def fa_check_device_status(stream=None) -> int:

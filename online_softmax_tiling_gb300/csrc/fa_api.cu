@@ -241,6 +241,52 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                     workspace, workspace_bytes);
 }
 
+// ---- split-KV without any allocation by the library or its caller --------
+// Some callers cannot call cudaMalloc: a plugin whose host framework owns all
+// device memory and forbids other allocations, or a latency-critical path that
+// cannot take cudaMalloc's implicit device synchronisation.  For them the
+// split-KV partials live in this fixed array, which every GPU that loads the
+// library holds until the process exits.  In host code the name is only a
+// host-side stand-in, so its device address is looked up per device.
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+// Device address of g_fa_noalloc_scratch on the current device, resolved on
+// the first call for that device (nullptr if the lookup fails).
+void* noalloc_scratch() {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[device] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_fa_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[device] = ptr;
+    }
+    return addr[device];
+}
+}  // namespace
+
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal, int dtype,
+                           int num_splits, void* stream) {
+    if (num_splits == 0) num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    if (num_splits == 1)
+        return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0);
+    if (fa_splitkv_workspace_size(B, H, N, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES)
+        return FA_ERR_UNSUPPORTED;
+    // Nothing in the partials needs to start at zero: every range writes both
+    // of its log-sums for every row, and the merge reads O only where they
+    // are finite.  Calls share the array, so calls that may overlap on the GPU
+    // race; callers must order them (one stream, or events).
+    void* scratch = noalloc_scratch();
+    if (scratch == nullptr) return FA_ERR_CUDA;
+    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0, num_splits,
+                    scratch, FA_NOALLOC_SCRATCH_BYTES);
+}
+
 int fa_check_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     unsigned int st = 0;
