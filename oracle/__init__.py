@@ -70,7 +70,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attention_f64.argtypes = [dp, dp, dp, i64, i64, i64, i64, ctypes.c_double,
                                          ctypes.c_int, dp, dp]
     lib.oracle_attention_f64.restype = ctypes.c_int
-    lib.oracle_attention_rows16.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64,
+    lib.oracle_attention_rows16.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64, i64,
                                             ctypes.c_double, ctypes.c_int, i64p, i64,
                                             dp, dp, dp, ctypes.c_int]
     lib.oracle_attention_rows16.restype = ctypes.c_int
@@ -86,6 +86,17 @@ def _ptr(a: np.ndarray | None, ctype):
     if a is None:
         return ctypes.cast(None, ctypes.POINTER(ctype))
     return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+NO_MASK, TOP_LEFT, BOTTOM_RIGHT = 0, 1, 2
+
+
+def _mask(causal) -> int:
+    """False/0: no mask; True/1: top-left causal; 2: bottom-right causal."""
+    m = int(causal)
+    if m not in (NO_MASK, TOP_LEFT, BOTTOM_RIGHT):
+        raise ValueError(f"mask mode {causal!r}")
+    return m
 
 
 def _f64(a) -> np.ndarray:
@@ -118,7 +129,7 @@ def attention(q, k, v, scale: float, causal: bool = False, lib: ctypes.CDLL | No
     lse = np.empty(q.shape[:-1], dtype=np.float64)
     rc = lib.oracle_attention_f64(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
                                   _ptr(v, ctypes.c_double), BH, Nq, Nk, d, float(scale),
-                                  int(bool(causal)), _ptr(o, ctypes.c_double),
+                                  _mask(causal), _ptr(o, ctypes.c_double),
                                   _ptr(lse, ctypes.c_double))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_f64 failed ({rc})")
@@ -130,19 +141,21 @@ def attention_rows16(q16, k16, v16, dtype: int, scale: float, causal: bool, rows
                      lib: ctypes.CDLL | None = None):
     """Plain definition for selected query rows of 16-bit inputs.
 
-    q16, k16, v16: uint16 bit patterns of shape [B, H, N, d] (or [BH, N, d]).
-    rows: flat row indices ``bh * N + i``.  Returns (O [nrows, d], LSE [nrows])
-    in float64, plus spread [nrows, d] = sum_j P_ij |v_jc - O_ic| when
-    ``with_spread`` (the sensitivity of O to relative errors in the weights).
+    q16: uint16 bit patterns [B, H, Nq, d] (or [BH, Nq, d]); k16, v16: the
+    same with Nk rows.  causal: mask mode (False, True = top-left, 2 =
+    bottom-right).  rows: flat row indices ``bh * Nq + i``.  Returns
+    (O [nrows, d], LSE [nrows]) in float64, plus spread [nrows, d] =
+    sum_j P_ij |v_jc - O_ic| when ``with_spread`` (the sensitivity of O to
+    relative errors in the weights).
     """
     lib = lib or load()
     q16 = np.ascontiguousarray(q16, dtype=np.uint16)
     k16 = np.ascontiguousarray(k16, dtype=np.uint16)
     v16 = np.ascontiguousarray(v16, dtype=np.uint16)
-    if not (q16.shape == k16.shape == v16.shape):
-        raise ValueError("q, k, v must share a shape")
-    N, d = q16.shape[-2], q16.shape[-1]
-    BH = q16.size // (N * d)
+    if k16.shape != v16.shape or q16.shape[:-2] != k16.shape[:-2] or q16.shape[-1] != k16.shape[-1]:
+        raise ValueError("q: [..., Nq, d]; k, v: [..., Nk, d]")
+    Nq, Nk, d = q16.shape[-2], k16.shape[-2], q16.shape[-1]
+    BH = q16.size // (Nq * d)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     order = np.argsort(rows, kind="stable")          # group rows of one head together
     srows = np.ascontiguousarray(rows[order])
@@ -152,8 +165,8 @@ def attention_rows16(q16, k16, v16, dtype: int, scale: float, causal: bool, rows
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
     rc = lib.oracle_attention_rows16(_ptr(q16, ctypes.c_uint16), _ptr(k16, ctypes.c_uint16),
-                                     _ptr(v16, ctypes.c_uint16), int(dtype), BH, N, d,
-                                     float(scale), int(bool(causal)),
+                                     _ptr(v16, ctypes.c_uint16), int(dtype), BH, Nq, Nk, d,
+                                     float(scale), _mask(causal),
                                      _ptr(srows, ctypes.c_int64), srows.size,
                                      _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
                                      _ptr(spread, ctypes.c_double), int(nthreads))
@@ -192,7 +205,7 @@ def blocked_head(q, k, v, scale: float, causal: bool, block_n: int, trace: bool 
               "e": np.empty((nblk, Nq, block_n))}
     rc = lib.oracle_blocked_head(
         _ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double), _ptr(v, ctypes.c_double),
-        Nq, Nk, d, float(scale), int(bool(causal)), int(block_n),
+        Nq, Nk, d, float(scale), _mask(causal), int(block_n),
         _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
         _ptr(tr["m"] if tr else None, ctypes.c_double),
         _ptr(tr["l"] if tr else None, ctypes.c_double),

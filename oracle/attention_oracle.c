@@ -22,10 +22,12 @@
  *     O[i]  = sum_j exp(s * (x_j - m)) * v[j] / l
  *     LSE_i = s * m + ln(l)                     ([QS] section "最后：归一化并写回 O")
  *   With Nq queries and Nk keys per head, key j is valid when j < Nk and, for
- *   the causal variant, j <= i (top-left alignment, [QS] section
- *   "causal 模式在哪一步生效", Fig. 11, whose worked example has 2 queries and
- *   4 keys).  A row with no valid key gets O = 0 and LSE = -inf (the pages
- *   leave this case open; it cannot occur when Nq <= Nk).
+ *   the causal variant, j <= i + offset: offset 0 is the top-left alignment of
+ *   [QS] section "causal 模式在哪一步生效", Fig. 11 (whose worked example has 2
+ *   queries and 4 keys); offset Nk - Nq is the bottom-right alignment that
+ *   section mentions without defining, read here as "the last query sees
+ *   every key".  Mask modes: 0 none, 1 top-left, 2 bottom-right.  A row with
+ *   no valid key gets O = 0 and LSE = -inf (the pages leave this case open).
  *
  * Subtracting the row maximum before exponentiating is the numerically stable
  * softmax of [PW] section 3.1; it does not change the value.
@@ -94,8 +96,17 @@ void oracle_decode16(const uint16_t* src, int dtype, double* dst, int64_t n) {
 
 /* ---- one query row, plain definition -------------------------------------- */
 
+/* Keys visible to query row i (a prefix 0 .. result-1 of the Nk keys). */
+static int64_t visible_keys(int mask, int64_t i, int64_t Nq, int64_t Nk) {
+    if (mask == 0) return Nk;
+    int64_t end = i + 1 + (mask == 2 ? Nk - Nq : 0);
+    if (end > Nk) end = Nk;
+    return end < 0 ? 0 : end;
+}
+
 /*
- * q: [d]; k, v: [Nk, d] of one (b, h); x: scratch of Nk doubles.
+ * q: [d]; k, v: [Nk, d] of one (b, h); the first nvalid keys are visible;
+ * x: scratch of Nk doubles.
  * spread (optional, [d]): sum_j P_ij |v_jc - O_ic|, the probability-weighted
  * spread of the values around the output.  It bounds how far O moves when
  * every weight is perturbed by a relative error of at most u: the change in
@@ -103,10 +114,8 @@ void oracle_decode16(const uint16_t* src, int dtype, double* dst, int64_t n) {
  * rounding of the weights to 16 bits before the P.V product.
  */
 static void attend_row(const double* q, const double* k, const double* v,
-                       int64_t Nk, int64_t d, double s, int causal, int64_t i,
+                       int64_t nvalid, int64_t d, double s,
                        double* x, double* o_row, double* lse_out, double* spread) {
-    int64_t nvalid = Nk;
-    if (causal && i + 1 < nvalid) nvalid = i + 1;
     if (nvalid <= 0) {
         for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
         if (spread)
@@ -148,7 +157,8 @@ static void attend_row(const double* q, const double* k, const double* v,
 
 /* ---- double inputs, whole tensors ----------------------------------------- */
 
-/* q, o: [BH, Nq, d]; k, v: [BH, Nk, d] doubles; lse: [BH, Nq]. Single-threaded. */
+/* q, o: [BH, Nq, d]; k, v: [BH, Nk, d] doubles; lse: [BH, Nq]; mask 0/1/2.
+ * Single-threaded. */
 int oracle_attention_f64(const double* q, const double* k, const double* v,
                          int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                          double scale, int causal, double* o, double* lse) {
@@ -160,7 +170,7 @@ int oracle_attention_f64(const double* q, const double* k, const double* v,
         const double* kh = k + bh * Nk * d;
         const double* vh = v + bh * Nk * d;
         for (int64_t i = 0; i < Nq; ++i)
-            attend_row(qh + i * d, kh, vh, Nk, d, scale, causal, i, x,
+            attend_row(qh + i * d, kh, vh, visible_keys(causal, i, Nq, Nk), d, scale, x,
                        o + (bh * Nq + i) * d, lse + bh * Nq + i, NULL);
     }
     free(x);
@@ -172,10 +182,10 @@ int oracle_attention_f64(const double* q, const double* k, const double* v,
 typedef struct {
     const uint16_t *q, *k, *v;
     int dtype;
-    int64_t N, d;
+    int64_t Nq, Nk, d;
     double scale;
-    int causal;
-    const int64_t* rows;   /* flat indices bh * N + i, sorted by bh for reuse */
+    int causal;            /* mask mode 0/1/2 */
+    const int64_t* rows;   /* flat indices bh * Nq + i, sorted by bh for reuse */
     int64_t nrows;
     double* o;             /* [nrows, d] */
     double* lse;           /* [nrows] */
@@ -189,11 +199,11 @@ typedef struct {
 
 static void* rows_worker(void* arg) {
     rows_job_t* job = (rows_job_t*)arg;
-    const int64_t N = job->N, d = job->d;
-    double* kh = (double*)malloc(sizeof(double) * (size_t)(N * d));
-    double* vh = (double*)malloc(sizeof(double) * (size_t)(N * d));
+    const int64_t Nq = job->Nq, Nk = job->Nk, d = job->d;
+    double* kh = (double*)malloc(sizeof(double) * (size_t)(Nk * d + 1));
+    double* vh = (double*)malloc(sizeof(double) * (size_t)(Nk * d + 1));
     double* qr = (double*)malloc(sizeof(double) * (size_t)d);
-    double* x = (double*)malloc(sizeof(double) * (size_t)N);
+    double* x = (double*)malloc(sizeof(double) * (size_t)(Nk + 1));
     if (!kh || !vh || !qr || !x) {
         pthread_mutex_lock(&job->lock);
         job->failed = 1;
@@ -211,14 +221,14 @@ static void* rows_worker(void* arg) {
         int64_t end = start + ROWS_CHUNK < job->nrows ? start + ROWS_CHUNK : job->nrows;
         for (int64_t r = start; r < end; ++r) {
             int64_t flat = job->rows[r];
-            int64_t bh = flat / N, i = flat % N;
+            int64_t bh = flat / Nq, i = flat % Nq;
             if (bh != cached_bh) {
-                oracle_decode16(job->k + bh * N * d, job->dtype, kh, N * d);
-                oracle_decode16(job->v + bh * N * d, job->dtype, vh, N * d);
+                oracle_decode16(job->k + bh * Nk * d, job->dtype, kh, Nk * d);
+                oracle_decode16(job->v + bh * Nk * d, job->dtype, vh, Nk * d);
                 cached_bh = bh;
             }
             oracle_decode16(job->q + flat * d, job->dtype, qr, d);
-            attend_row(qr, kh, vh, N, d, job->scale, job->causal, i, x,
+            attend_row(qr, kh, vh, visible_keys(job->causal, i, Nq, Nk), d, job->scale, x,
                        job->o + r * d, job->lse + r,
                        job->spread ? job->spread + r * d : NULL);
         }
@@ -228,24 +238,25 @@ static void* rows_worker(void* arg) {
 }
 
 /*
- * q, k, v: [BH, N, d] raw 16-bit patterns of `dtype`.  rows: nrows flat row
- * indices (bh * N + i), each in [0, BH * N).  o: [nrows, d], lse: [nrows],
- * spread: [nrows, d] or NULL (see attend_row).  Returns 0 on success.
+ * q: [BH, Nq, d], k, v: [BH, Nk, d] raw 16-bit patterns of `dtype`; mask
+ * mode 0/1/2.  rows: nrows flat row indices (bh * Nq + i), each in
+ * [0, BH * Nq).  o: [nrows, d], lse: [nrows], spread: [nrows, d] or NULL (see
+ * attend_row).  Returns 0 on success.
  */
 int oracle_attention_rows16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                            int dtype, int64_t BH, int64_t N, int64_t d,
+                            int dtype, int64_t BH, int64_t Nq, int64_t Nk, int64_t d,
                             double scale, int causal,
                             const int64_t* rows, int64_t nrows,
                             double* o, double* lse, double* spread, int nthreads) {
-    if (BH <= 0 || N <= 0 || d <= 0 || nrows < 0) return 1;
+    if (BH <= 0 || Nq <= 0 || Nk <= 0 || d <= 0 || nrows < 0) return 1;
     if (dtype != ORACLE_FP16 && dtype != ORACLE_BF16) return 1;
     for (int64_t r = 0; r < nrows; ++r)
-        if (rows[r] < 0 || rows[r] >= BH * N) return 1;
+        if (rows[r] < 0 || rows[r] >= BH * Nq) return 1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     rows_job_t job;
     job.q = q; job.k = k; job.v = v; job.dtype = dtype;
-    job.N = N; job.d = d; job.scale = scale; job.causal = causal;
+    job.Nq = Nq; job.Nk = Nk; job.d = d; job.scale = scale; job.causal = causal;
     job.rows = rows; job.nrows = nrows; job.o = o; job.lse = lse; job.spread = spread;
     job.next = 0; job.failed = 0;
     pthread_mutex_init(&job.lock, NULL);
@@ -304,7 +315,8 @@ int oracle_blocked_head(const double* q, const double* k, const double* v,
             int64_t j1 = j0 + block_n < Nk ? j0 + block_n : Nk;
             /* valid keys of this block */
             int64_t jend = j1;
-            if (causal && i + 1 < jend) jend = i + 1;
+            const int64_t vis = visible_keys(causal, i, Nq, Nk);
+            if (vis < jend) jend = vis;
             double alpha = NAN;
             if (trace_e)
                 for (int64_t jj = 0; jj < block_n; ++jj) trace_e[(t * Nq + i) * block_n + jj] = 0.0;

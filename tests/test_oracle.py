@@ -244,3 +244,91 @@ def test_spread_matches_brute_force_and_closed_form():
     _, _, sp = oracle.attention_rows16(qq, qq, vv, oracle.FP16, 1.0, False, [0, 1],
                                        with_spread=True)
     np.testing.assert_allclose(sp, [[1.0, 1.25], [1.0, 1.25]], atol=1e-15)
+
+
+def test_worked_example_bottom_right():
+    ex = _ex()
+    br = fixtures.load("worked_example_bottom_right.txt")
+    o, lse = oracle.attention(ex["Q"], ex["K"], ex["V"], br["scale"], oracle.BOTTOM_RIGHT)
+    np.testing.assert_allclose(o, br["O"], atol=EXACT)
+    np.testing.assert_allclose(lse, br["LSE"], atol=EXACT)
+    ob, lb = oracle.blocked_head(ex["Q"], ex["K"], ex["V"], br["scale"], oracle.BOTTOM_RIGHT, 2)
+    np.testing.assert_allclose(ob, br["O"], atol=EXACT)
+    np.testing.assert_allclose(lb, br["LSE"], atol=EXACT)
+
+
+def test_bottom_right_special_cases():
+    rng = np.random.default_rng(29)
+    # equal lengths: bottom-right is top-left
+    q, k, v, s = _rand_case(rng, 9, 4)
+    a = oracle.attention(q, k, v, s, oracle.TOP_LEFT)
+    b = oracle.attention(q, k, v, s, oracle.BOTTOM_RIGHT)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    # one query (decoding): it sees every key
+    q1 = rng.standard_normal((1, 4))
+    a = oracle.attention(q1, k, v, s, oracle.NO_MASK)
+    b = oracle.attention(q1, k, v, s, oracle.BOTTOM_RIGHT)
+    np.testing.assert_array_equal(a[0], b[0])
+    # more queries than keys: the first Nq - Nk rows see nothing, the next sees key 0
+    q7 = rng.standard_normal((7, 4))
+    k3, v3 = k[:3], v[:3]
+    o, lse = oracle.attention(q7, k3, v3, s, oracle.BOTTOM_RIGHT)
+    np.testing.assert_array_equal(o[:4], 0.0)
+    assert np.all(np.isneginf(lse[:4]))
+    np.testing.assert_allclose(o[4], v3[0], atol=1e-15)
+    assert abs(lse[4] - s * float(q7[4] @ k3[0])) < 1e-14
+
+
+@pytest.mark.parametrize("nq,nk", [(3, 8), (8, 3), (5, 5), (1, 9), (9, 1)])
+def test_recurrence_equals_plain_definition_unequal_lengths(nq, nk):
+    rng = np.random.default_rng(100 + nq * 10 + nk)
+    q = rng.standard_normal((nq, 3))
+    k = rng.standard_normal((nk, 3))
+    v = rng.standard_normal((nk, 3))
+    for mask in (oracle.NO_MASK, oracle.TOP_LEFT, oracle.BOTTOM_RIGHT):
+        o_ref, lse_ref = oracle.attention(q, k, v, 0.6, mask)
+        for bn in range(1, nk + 2):
+            o, lse = oracle.blocked_head(q, k, v, 0.6, mask, bn)
+            np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+            np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(lse_ref))
+            fin = np.isfinite(lse_ref)
+            np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=0, atol=1e-12)
+
+
+def test_brute_force_unequal_lengths_bottom_right():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(37)
+    for nq, nk in [(3, 7), (6, 4), (1, 5)]:
+        q = rng.standard_normal((nq, 3))
+        k = rng.standard_normal((nk, 3))
+        v = rng.standard_normal((nk, 3))
+        o, lse = oracle.attention(q, k, v, 0.9, oracle.BOTTOM_RIGHT)
+        for i in range(nq):
+            nv = min(nk, max(0, i + 1 + nk - nq))
+            if nv == 0:
+                assert np.all(o[i] == 0) and np.isneginf(lse[i])
+                continue
+            ws = [mpmath.exp(mpmath.mpf(0.9) * mpmath.fsum(mpmath.mpf(q[i, c]) * mpmath.mpf(k[j, c])
+                                                         for c in range(3))) for j in range(nv)]
+            tot = mpmath.fsum(ws)
+            for c in range(3):
+                ref = mpmath.fsum(w * mpmath.mpf(v[j, c]) for j, w in enumerate(ws)) / tot
+                assert abs(float(ref) - o[i, c]) < 1e-13
+            assert abs(float(mpmath.log(tot)) - lse[i]) < 1e-13
+
+
+def test_rows16_unequal_lengths_match_widened_definition():
+    from online_softmax_tiling_gb300 import synth
+    dtype = oracle.BF16
+    q = synth.tensor_bits(301, (1, 2, 13, 8), dtype)
+    k = synth.tensor_bits(302, (1, 2, 29, 8), dtype)
+    v = synth.tensor_bits(303, (1, 2, 29, 8), dtype)
+    for mask in (oracle.NO_MASK, oracle.TOP_LEFT, oracle.BOTTOM_RIGHT):
+        o_all, lse_all = oracle.attention(oracle.decode16(q, dtype), oracle.decode16(k, dtype),
+                                          oracle.decode16(v, dtype), 0.3, mask)
+        rows = np.arange(26, dtype=np.int64)
+        o, lse = oracle.attention_rows16(q, k, v, dtype, 0.3, mask, rows)
+        np.testing.assert_array_equal(o, o_all.reshape(-1, 8))
+        np.testing.assert_array_equal(lse, lse_all.reshape(-1))

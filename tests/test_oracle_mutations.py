@@ -19,8 +19,10 @@ MUTATIONS = {
     "exponent_sign": ("double w = exp(s * (x[j] - m));", "double w = exp(s * (m - x[j]));"),
     "spread_drops_abs": ("spread[c] += p * fabs(vj[c] - o_row[c]);",
                          "spread[c] += p * (vj[c] - o_row[c]);"),
-    "causal_off_by_one": ("if (causal && i + 1 < nvalid) nvalid = i + 1;",
-                          "if (causal && i < nvalid) nvalid = i;"),
+    "causal_off_by_one": ("int64_t end = i + 1 + (mask == 2 ? Nk - Nq : 0);",
+                          "int64_t end = i + (mask == 2 ? Nk - Nq : 0);"),
+    "bottom_right_offset_sign": ("int64_t end = i + 1 + (mask == 2 ? Nk - Nq : 0);",
+                                 "int64_t end = i + 1 + (mask == 2 ? Nq - Nk : 0);"),
     "no_normalisation": ("for (int64_t c = 0; c < d; ++c) o_row[c] /= l;",
                          "for (int64_t c = 0; c < d; ++c) o_row[c] /= 1.0;"),
     "wrong_value_row": ("l += w;\n        const double* vj = v + j * d;",
@@ -57,6 +59,10 @@ def _pins(lib) -> list:
     o, lse = oracle.attention(ex["Q"], ex["K"], ex["V"], cz["scale"], True, lib=lib)
     check("worked_causal", np.allclose(o, cz["O"], atol=1e-14)
           and np.allclose(lse, cz["LSE"], atol=1e-14))
+    br = fixtures.load("worked_example_bottom_right.txt")
+    o, lse = oracle.attention(ex["Q"], ex["K"], ex["V"], br["scale"], oracle.BOTTOM_RIGHT, lib=lib)
+    check("worked_bottom_right", np.allclose(o, br["O"], atol=1e-14)
+          and np.allclose(lse, br["LSE"], atol=1e-14))
     o, lse, tr = oracle.blocked_head(ex["Q"], ex["K"], ex["V"], ex["scale"], False, 2,
                                      trace=True, lib=lib)
     check("worked_recurrence", np.allclose(tr["l"][1], ex["l1"], atol=1e-14)
