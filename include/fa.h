@@ -72,6 +72,53 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            void* stream);
 
 /*
+ * fa_fwd_ex - the general form: separate query and key lengths, strided
+ * tensors, three masks, optional split-KV.  Fields of fa_fwd_args:
+ *   q [B, H, Nq, d], k and v [B, H, Nk, d], o [B, H, Nq, d]: 16-bit device
+ *     tensors, d contiguous; *_stride = {batch, head, row} strides in
+ *     elements, each a positive multiple of 8 (16 bytes, a TMA rule), e.g.
+ *     {H*N*d, N*d, d} for [B, H, N, d] or {N*H*d, d, H*d} for [B, N, H, d].
+ *     Base pointers 16-byte aligned (else FA_ERR_MISALIGNED).
+ *   lse [B, H, Nq] fp32 with rows contiguous and lse_stride = {batch, head}.
+ *   mask: FA_MASK_NONE; FA_MASK_CAUSAL_TOP_LEFT (key j visible to query i
+ *     iff j <= i, section "causal 模式在哪一步生效", Fig. 11); or
+ *     FA_MASK_CAUSAL_BOTTOM_RIGHT (j <= i + Nk - Nq, the alignment that
+ *     section mentions for unequal lengths: the last query sees every key).
+ *     A query that sees no key gets O = 0 and LSE = -inf.
+ *   num_splits, workspace, workspace_bytes: as fa_fwd_splitkv (1 = none;
+ *     the workspace size is fa_splitkv_workspace_size(B, H, Nq, d, splits)).
+ *   scale, dtype, stream: as fa_fwd.
+ * fa_fwd(...) is fa_fwd_ex with contiguous strides, Nq = Nk = N and the
+ * top-left mask when `causal`.
+ */
+#define FA_MASK_NONE 0
+#define FA_MASK_CAUSAL_TOP_LEFT 1
+#define FA_MASK_CAUSAL_BOTTOM_RIGHT 2
+
+typedef struct fa_fwd_args {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int B, H, Nq, Nk, d;
+    long long q_stride[3];
+    long long k_stride[3];
+    long long v_stride[3];
+    long long o_stride[3];
+    long long lse_stride[2];
+    float scale;
+    int mask;
+    int dtype;
+    int num_splits;
+    void* workspace;
+    size_t workspace_bytes;
+    void* stream;
+} fa_fwd_args;
+
+int fa_fwd_ex(const fa_fwd_args* args);
+
+/*
  * Split-KV ("CUDA 算子工程" ch. 14, section 14.7.1): when B*H*ceil(N/256) query
  * blocks cannot fill the GPU, the key tiles of every block are divided into
  * num_splits contiguous ranges processed by separate CTAs; each writes a

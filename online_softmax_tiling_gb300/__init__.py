@@ -24,7 +24,22 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
 EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug",
            "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv",
-           "fa_fwd_splitkv_noalloc")
+           "fa_fwd_splitkv_noalloc", "fa_fwd_ex")
+FA_MASK_NONE, FA_MASK_CAUSAL_TOP_LEFT, FA_MASK_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+
+
+class fa_fwd_args(ctypes.Structure):
+    """Mirror of `fa_fwd_args` in include/fa.h (same field order and types)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("B", ctypes.c_int), ("H", ctypes.c_int), ("Nq", ctypes.c_int),
+                ("Nk", ctypes.c_int), ("d", ctypes.c_int),
+                ("q_stride", ctypes.c_longlong * 3), ("k_stride", ctypes.c_longlong * 3),
+                ("v_stride", ctypes.c_longlong * 3), ("o_stride", ctypes.c_longlong * 3),
+                ("lse_stride", ctypes.c_longlong * 2),
+                ("scale", ctypes.c_float), ("mask", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("num_splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("stream", ctypes.c_void_p)]
 FA_NOALLOC_SCRATCH_BYTES = 16 << 20
 FA_MAX_SPLITS = 32
 
@@ -70,6 +85,8 @@ def library() -> ctypes.CDLL:
             lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float,
                                                    i, i, i, vp]
             lib.fa_fwd_splitkv_noalloc.restype = i
+            lib.fa_fwd_ex.argtypes = [ctypes.POINTER(fa_fwd_args)]
+            lib.fa_fwd_ex.restype = i
             _lib = lib
         return _lib
 
@@ -110,6 +127,11 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nu
     return library().fa_fwd_splitkv_noalloc(q, k, v, o, lse, int(B), int(H), int(N), int(d),
                                             float(scale), int(causal), int(dtype),
                                             int(num_splits), stream)
+
+
+def fa_fwd_ex(args: "fa_fwd_args") -> int:
+    """Raw C call of the general entry point with a filled `fa_fwd_args`."""
+    return library().fa_fwd_ex(ctypes.byref(args))
 
 
 def fa_check_device_status(stream=None) -> int:
@@ -176,4 +198,56 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
                             ws.data_ptr(), nbytes, handle)
     if st != FA_OK:
         raise FaError(st)
+    return out, lse
+
+
+def attention_forward_ex(q, k, v, scale: float | None = None, mask: int = FA_MASK_NONE,
+                         out=None, lse=None, stream=None, num_splits: int = 1):
+    """General form for CUDA tensors q [B, H, Nq, d], k, v [B, H, Nk, d] of any
+    strides with d contiguous (e.g. transposed views of [B, N, H, d] data).
+
+    mask: FA_MASK_NONE, FA_MASK_CAUSAL_TOP_LEFT or FA_MASK_CAUSAL_BOTTOM_RIGHT.
+    out (O, [B, H, Nq, d]) and lse ([B, H, Nq], rows contiguous) may be strided
+    too; they are allocated contiguous when not given.  num_splits as in
+    attention_forward.
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError("q: [B, H, Nq, d]; k, v: [B, H, Nk, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not t.is_cuda or t.stride(3) != 1:
+            raise ValueError(f"{name} must be a CUDA tensor with a contiguous last dimension")
+    if not lse.is_cuda or lse.stride(2) != 1:
+        raise ValueError("lse must be a CUDA tensor with contiguous rows")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    a = fa_fwd_args()
+    a.q, a.k, a.v, a.o, a.lse = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), \
+        lse.data_ptr()
+    a.B, a.H, a.Nq, a.Nk, a.d = B, H, Nq, Nk, d
+    for field, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", out)):
+        getattr(a, field)[:] = [t.stride(0), t.stride(1), t.stride(2)]
+    a.lse_stride[:] = [lse.stride(0), lse.stride(1)]
+    a.scale, a.mask, a.dtype = float(scale), int(mask), _dtype_code(q)
+    if num_splits == 0:
+        num_splits = fa_splitkv_num_splits(B, H, Nq, d, int(mask != FA_MASK_NONE))
+    a.num_splits = num_splits
+    ws = None
+    if num_splits > 1:
+        a.workspace_bytes = fa_splitkv_workspace_size(B, H, Nq, d, num_splits)
+        ws = torch.empty(a.workspace_bytes, dtype=torch.uint8, device=q.device)
+        a.workspace = ws.data_ptr()
+    a.stream = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    st = fa_fwd_ex(a)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_ex")
     return out, lse

@@ -39,22 +39,25 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B*H, N, d] 16-bit tensor viewed in 3-D so that rows >= N of one head are
-// out of range (zero-filled on load, clipped on store) instead of belonging
-// to the next head.  Box: 64 columns (128 bytes, one swizzle span) x 128 rows
-// (one query tile, one key tile).
-bool encode_qkvo(CUtensorMap* map, const void* ptr, int dtype, int64_t BH, int64_t N, int64_t d) {
+// A 16-bit [B, H, rows, d] tensor with element strides (batch, head, row) and
+// contiguous d, viewed by TMA in 4-D (d, rows, H, B) so that rows >= `rows`
+// of one head are out of range (zero-filled on load, clipped on store)
+// instead of belonging to the next head.  Box: 64 columns (128 bytes, one
+// swizzle span) x 128 rows (one query tile or one key tile) x 1 x 1.
+bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t H, int64_t rows,
+               int64_t d, const long long (&stride)[3]) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(stride[2]) * 2,
+                                   static_cast<cuuint64_t>(stride[1]) * 2,
+                                   static_cast<cuuint64_t>(stride[0]) * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    return fn(map, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -120,73 +123,121 @@ size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
     return split_o_bytes(S, BH, N, d) + static_cast<size_t>(2 * S * BH * N) * 4;
 }
 
-int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-             int N, int d, float scale, int causal, int dtype, void* stream, int fault_mode,
-             double timeout_s, int num_splits = 1, void* workspace = nullptr,
-             size_t workspace_bytes = 0) {
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+// Contiguous [B, H, N, d] strides.
+fa_fwd_args contiguous_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int H, int N, int d, float scale, int causal, int dtype, void* stream) {
+    fa_fwd_args a{};
+    a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+    a.B = B; a.H = H; a.Nq = N; a.Nk = N; a.d = d;
+    const long long sn = d, sh = static_cast<long long>(N) * d, sb = sh * H;
+    for (long long* st : {a.q_stride, a.k_stride, a.v_stride, a.o_stride}) {
+        st[0] = sb; st[1] = sh; st[2] = sn;
+    }
+    a.lse_stride[0] = static_cast<long long>(H) * N;
+    a.lse_stride[1] = N;
+    a.scale = scale;
+    a.mask = causal ? FA_MASK_CAUSAL_TOP_LEFT : FA_MASK_NONE;
+    a.dtype = dtype;
+    a.num_splits = 1;
+    a.stream = stream;
+    return a;
+}
+
+int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
+    const int B = a.B, H = a.H, Nq = a.Nq, Nk = a.Nk, d = a.d, dtype = a.dtype;
+    if (!a.q || !a.k || !a.v || !a.o || !a.lse) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (a.mask != FA_MASK_NONE && a.mask != FA_MASK_CAUSAL_TOP_LEFT &&
+        a.mask != FA_MASK_CAUSAL_BOTTOM_RIGHT)
+        return FA_ERR_INVALID_ARG;
     if (!(timeout_s > 0.0) || !std::isfinite(timeout_s)) return FA_ERR_INVALID_ARG;
     if (fault_mode < 0 || fault_mode > 1) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    const int64_t nq = (static_cast<int64_t>(N) + fa::kBlockM - 1) / fa::kBlockM;  // CTAs per head
+    const int64_t nq = (static_cast<int64_t>(Nq) + fa::kBlockM - 1) / fa::kBlockM;  // CTAs per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
-    auto misaligned = [](const void* ptr, uintptr_t a) {
-        return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0;
+    // TMA: every stride a positive multiple of 16 bytes (8 16-bit elements);
+    // LSE rows contiguous, its strides positive
+    for (const long long* st : {a.q_stride, a.k_stride, a.v_stride, a.o_stride})
+        for (int i = 0; i < 3; ++i)
+            if (st[i] <= 0 || st[i] % 8 != 0 || st[i] >= (1ll << 39)) return FA_ERR_MISALIGNED;
+    if (a.lse_stride[0] <= 0 || a.lse_stride[1] <= 0) return FA_ERR_INVALID_ARG;
+    auto misaligned = [](const void* ptr, uintptr_t al) {
+        return (reinterpret_cast<uintptr_t>(ptr) & (al - 1)) != 0;
     };
-    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
-        misaligned(lse, 4))
+    if (misaligned(a.q, 16) || misaligned(a.k, 16) || misaligned(a.v, 16) || misaligned(a.o, 16) ||
+        misaligned(a.lse, 4))
         return FA_ERR_MISALIGNED;
-    const bool split = num_splits > 1;
+    int num_splits = a.num_splits;
+    if (num_splits == 0)
+        num_splits = fa_splitkv_num_splits(B, H, Nq, d, a.mask != FA_MASK_NONE);
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    const bool split = num_splits > 1;
     if (split) {
-        if (!workspace) return FA_ERR_INVALID_ARG;
-        if (misaligned(workspace, 256)) return FA_ERR_MISALIGNED;
-        if (workspace_bytes < split_workspace_bytes(num_splits, BH, N, d)) return FA_ERR_INVALID_ARG;
+        if (!a.workspace) return FA_ERR_INVALID_ARG;
+        if (misaligned(a.workspace, 256)) return FA_ERR_MISALIGNED;
+        if (a.workspace_bytes < split_workspace_bytes(num_splits, BH, Nq, d)) return FA_ERR_INVALID_ARG;
         if (BH * nq * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
     }
 
     CUtensorMap tq, tk, tv, to;
-    if (!encode_qkvo(&tq, q, dtype, BH, N, d) || !encode_qkvo(&tk, k, dtype, BH, N, d) ||
-        !encode_qkvo(&tv, v, dtype, BH, N, d) || !encode_qkvo(&to, o, dtype, BH, N, d))
+    if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride) ||
+        !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride) ||
+        !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride) ||
+        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride))
         return FA_ERR_CUDA;
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
-    const KernelEntry ke = select_kernel(d, dtype, causal != 0, split);
+    const bool causal = a.mask != FA_MASK_NONE;
+    const KernelEntry ke = select_kernel(d, dtype, causal, split);
     if (!ensure_smem_attr(ke.fn, ke.smem, device)) return FA_ERR_CUDA;
 
     fa::FwdParams prm;
-    prm.lse = lse;
-    prm.N = N;
+    prm.lse = a.lse;
+    prm.lse_sb = a.lse_stride[0];
+    prm.lse_sh = a.lse_stride[1];
+    prm.Nq = Nq;
+    prm.Nk = Nk;
+    prm.H = H;
+    prm.mask_offset = a.mask == FA_MASK_CAUSAL_BOTTOM_RIGHT ? Nk - Nq : 0;
     prm.num_q_blocks = static_cast<int>(nq);
-    prm.scale = scale;
-    prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    prm.scale = a.scale;
+    prm.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
     prm.timeout_ns = static_cast<unsigned long long>(timeout_s * 1e9);
     prm.fault_mode = fault_mode;
     prm.num_splits = num_splits;
     prm.BH = static_cast<int>(BH);
-    prm.o_part = split ? static_cast<float*>(workspace) : nullptr;
-    prm.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                    split_o_bytes(num_splits, BH, N, d))
+    prm.o_part = split ? static_cast<float*>(a.workspace) : nullptr;
+    prm.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(a.workspace) +
+                                                    split_o_bytes(num_splits, BH, Nq, d))
                          : nullptr;
 
     void* args[] = {&tq, &tk, &tv, &to, &prm};
     const dim3 grid(static_cast<unsigned>(BH * nq * num_splits));
     const dim3 block(fa::kThreads);
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaStream_t st = static_cast<cudaStream_t>(a.stream);
     if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem), st) != cudaSuccess)
         return FA_ERR_CUDA;
     if (split) {
-        const long long rows = static_cast<long long>(BH) * N;
-        const float* op = prm.o_part;
-        const float* lp = prm.lse_part;
-        void* margs[] = {const_cast<float**>(&op), const_cast<float**>(&lp), &o, &lse,
-                         &num_splits, const_cast<long long*>(&rows)};
-        const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));
+        fa::MergeParams mp;
+        mp.o_part = prm.o_part;
+        mp.lse_part = prm.lse_part;
+        mp.o = a.o;
+        mp.o_sb = a.o_stride[0];
+        mp.o_sh = a.o_stride[1];
+        mp.o_sn = a.o_stride[2];
+        mp.lse = a.lse;
+        mp.lse_sb = a.lse_stride[0];
+        mp.lse_sh = a.lse_stride[1];
+        mp.num_splits = num_splits;
+        mp.H = H;
+        mp.Nq = Nq;
+        mp.rows = BH * Nq;
+        void* margs[] = {&mp};
+        const dim3 mgrid(static_cast<unsigned>((mp.rows + 7) / 8));
         if (cudaLaunchKernel(select_merge(d, dtype), mgrid, dim3(256), margs, 0, st) != cudaSuccess)
             return FA_ERR_CUDA;
     }
@@ -199,14 +250,20 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, int dtype, void* stream) {
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0);
+    return fwd_core(contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream), 0,
+                    2.0);
+}
+
+int fa_fwd_ex(const fa_fwd_args* args) {
+    if (!args) return FA_ERR_INVALID_ARG;
+    return fwd_core(*args, 0, 2.0);
 }
 
 int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, int dtype, void* stream, int fault_mode,
                  double timeout_s) {
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, fault_mode,
-                    timeout_s);
+    return fwd_core(contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream),
+                    fault_mode, timeout_s);
 }
 
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
@@ -236,9 +293,11 @@ size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, float scale, int causal, int dtype, int num_splits,
                    void* workspace, size_t workspace_bytes, void* stream) {
-    if (num_splits == 0) num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0, num_splits,
-                    workspace, workspace_bytes);
+    fa_fwd_args a = contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
+    a.num_splits = num_splits;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return fwd_core(a, 0, 2.0);
 }
 
 // ---- split-KV without any allocation by the library or its caller --------
@@ -273,8 +332,8 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
                            int num_splits, void* stream) {
     if (num_splits == 0) num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
-    if (num_splits == 1)
-        return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0);
+    fa_fwd_args a = contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
+    if (num_splits == 1) return fwd_core(a, 0, 2.0);
     if (fa_splitkv_workspace_size(B, H, N, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES)
         return FA_ERR_UNSUPPORTED;
     // Nothing in the partials needs to start at zero: every range writes both
@@ -283,8 +342,10 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
     // race; callers must order them (one stream, or events).
     void* scratch = noalloc_scratch();
     if (scratch == nullptr) return FA_ERR_CUDA;
-    return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream, 0, 2.0, num_splits,
-                    scratch, FA_NOALLOC_SCRATCH_BYTES);
+    a.num_splits = num_splits;
+    a.workspace = scratch;
+    a.workspace_bytes = FA_NOALLOC_SCRATCH_BYTES;
+    return fwd_core(a, 0, 2.0);
 }
 
 int fa_check_device_status(void* stream) {

@@ -68,15 +68,18 @@ constexpr uint32_t kTmemU = 256;      // U_A at 256, U_B at 384
 __device__ unsigned int g_fa_status;
 
 struct FwdParams {
-    float* lse;
-    int N;
-    int num_q_blocks;  // ceil(N / 256)
+    float* lse;               // LSE of (b, h, row) at lse + b lse_sb + h lse_sh + row
+    long long lse_sb, lse_sh;
+    int Nq, Nk;               // query rows and keys per (b, h)
+    int H;                    // heads (bh = b H + h)
+    int mask_offset;          // causal: key j visible to row i iff j <= i + mask_offset
+    int num_q_blocks;  // ceil(Nq / 256)
     // split-KV only: key tiles of each query block are divided into
     // num_splits contiguous ranges; each CTA writes a partial result
     int num_splits;
     int BH;
-    float* o_part;    // [num_splits][BH][N][d] fp32, O of the range (normalised by its lhat)
-    float* lse_part;  // [2][num_splits][BH][N] fp32: LSE of the range, and its log-sum of
+    float* o_part;    // [num_splits][BH][Nq][d] fp32, O of the range (normalised by its lhat)
+    float* lse_part;  // [2][num_splits][BH][Nq] fp32: LSE of the range, and its log-sum of
                       // the rounded weights (the weight of its O in the merge)
     float scale;       // s
     float scale_log2;  // s * log2(e): exp(s x) = 2^(x * scale_log2)
@@ -237,10 +240,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = blk / p.num_q_blocks;
     int qb = blk % p.num_q_blocks;
     if (CAUSAL) qb = p.num_q_blocks - 1 - qb;
-    const int nkv = (p.N + kBlockN - 1) / kBlockN;
-    // key tiles visible to query tile A (rows qb*256 + [0,128)) and B ([128,256))
-    const int T_A = CAUSAL ? min(2 * qb + 1, nkv) : nkv;
-    const int T_B = CAUSAL ? min(2 * qb + 2, nkv) : nkv;
+    const int b_idx = bh / p.H, h_idx = bh % p.H;
+    const int nkv = (p.Nk + kBlockN - 1) / kBlockN;
+    // key tiles visible to query tile A (rows qb*256 + [0,128)) and B ([128,256)):
+    // with the causal mask, up to the tile holding key (last row + offset)
+    auto visible_tiles = [&](int x) {
+        if (!CAUSAL) return nkv;
+        const int last = min(qb * kBlockM + x * kTileM + kTileM - 1, p.Nq - 1) + p.mask_offset;
+        return last < 0 ? 0 : min(last / kBlockN + 1, nkv);
+    };
+    const int T_A = visible_tiles(0);
+    const int T_B = visible_tiles(1);
     // this CTA visits key tiles k0 .. k0 + n_x - 1 for tile x (all of them
     // unless split-KV divides the range of the block into num_splits parts)
     int k0 = 0, nA = T_A, nB = T_B;
@@ -252,9 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         nA = max(0, min(k1, T_A) - k0);
         if (nB == 0) {  // empty range: its partials carry no weight
             const int row = qb * kBlockM + static_cast<int>(threadIdx.x);
-            if (threadIdx.x < kBlockM && row < p.N) {
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.N + row;
-                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.N;
+            if (threadIdx.x < kBlockM && row < p.Nq) {
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
                 p.lse_part[i] = -INFINITY;
                 p.lse_part[plane + i] = -INFINITY;
             }
@@ -324,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < 2; ++x)
 #pragma unroll
                 for (int c = 0; c < C::kSub; ++c)
-                    ptx::tma_load_3d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
-                                     qb * kBlockM + x * kTileM, bh);
+                    ptx::tma_load_4d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
+                                     qb * kBlockM + x * kTileM, h_idx, b_idx);
         }
         for (int j = 0; j <= nB; ++j) {
             if (j < nB) {
@@ -336,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(bar_kf(s), C::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_3d(sK(s) + c * kSubBytes, &tm_k, bar_kf(s), 64 * c,
-                                         (k0 + j) * kBlockN, bh);
+                        ptx::tma_load_4d(sK(s) + c * kSubBytes, &tm_k, bar_kf(s), 64 * c,
+                                         (k0 + j) * kBlockN, h_idx, b_idx);
                 }
                 if (!skip) ++issued_k[s];
             }
@@ -349,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(bar_vf(s), C::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_3d(sV(s) + c * kSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                         (k0 + jv) * kBlockN, bh);
+                        ptx::tma_load_4d(sV(s) + c * kSubBytes, &tm_v, bar_vf(s), 64 * c,
+                                         (k0 + jv) * kBlockN, h_idx, b_idx);
                 }
                 ++issued_v[s];
             }
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_ts_k128(tmem + kTmemU + x * 128, tmem + x * 128, v_desc0 + s * kTileStep,
                              idesc_pv, acc ? 1u : 0u);
         };
-        bool ok = wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
+        bool ok = nB > 0 && wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
         if (ok) {
             ptx::tc_fence_after_sync();
             if (nA > 0) {
@@ -440,14 +450,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = threadIdx.x & 127;                  // row in the tile = TMEM lane
         const int row = qb * kBlockM + x * kTileM + t;    // query index in the head
         const int T = x == 0 ? nA : nB;          // key tiles this CTA visits for the tile
-        const int T_all = x == 0 ? T_A : T_B;    // key tiles visible to the tile
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + x * 128;
         const uint32_t u_addr = tmem + lane_off + kTmemU + x * 128;
         const float c2 = p.scale_log2;
         const float2 c2v = make_float2(c2, c2);
-        // this row's 128 scores of the current tile, with keys >= N and, on the
-        // diagonal tile, keys in the future masked to -inf
+        // whether key tile j (local index) holds a key some row of this tile
+        // may not see: keys >= Nk, or keys past the causal limit of the tile's
+        // first row (with a bottom-right offset that can be two tiles)
+        const int first_row = qb * kBlockM + x * kTileM;
+        auto tile_masked = [&](int j) {
+            const int kend = (k0 + j + 1) * kBlockN;
+            return kend > p.Nk || (CAUSAL && kend - 1 > first_row + p.mask_offset);
+        };
+        // key limit (exclusive) of this row relative to `kbase`
+        auto key_limit = [&](int kbase) {
+            int limit = p.Nk - kbase;
+            if (CAUSAL) limit = min(limit, row + p.mask_offset - kbase + 1);
+            return limit;
+        };
+        // this row's 128 scores of the current tile, with the keys it may not
+        // see (>= Nk, or past the causal limit) masked to -inf
         auto load_scores = [&](uint32_t(&sv)[kBlockN], int j) {
 #pragma unroll
             for (int c = 0; c < kBlockN / 32; ++c)
@@ -456,10 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) ptx::reg_fence(sv[c]);
-            if (k0 + j == T_all - 1) {
-                const int kbase = (k0 + j) * kBlockN;
-                int limit = p.N - kbase;
-                if (CAUSAL) limit = min(limit, row - kbase + 1);
+            if (tile_masked(j)) {
+                const int limit = key_limit((k0 + j) * kBlockN);
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= limit) sv[c] = __float_as_uint(-INFINITY);
@@ -486,10 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int u = 0; u < 32; ++u) ptx::reg_fence(sv[u]);
-            if (k0 + j == T_all - 1) {
-                const int kbase = (k0 + j) * kBlockN + c * 32;
-                int limit = p.N - kbase;
-                if (CAUSAL) limit = min(limit, row - kbase + 1);
+            if (tile_masked(j)) {
+                const int limit = key_limit((k0 + j) * kBlockN + c * 32);
 #pragma unroll
                 for (int u = 0; u < 32; ++u)
                     if (u >= limit) sv[u] = __float_as_uint(-INFINITY);
@@ -591,6 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- epilogue: O = U / lhat -> 16-bit -> swizzled smem -> TMA store
         if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (T - 1) & 1, abort, tmo);
+        // a tile that sees no key stages its zeros over the Q tile: wait until
+        // the copy of Q has landed, or it could overwrite them
+        if (!SPLIT && !aborted && T == 0) aborted = !wait_warp(bar_q, 0, abort, tmo);
         const float l_all = lsum.x + lsum.y;
         const float lhat_all = lhat.x + lhat.y;
         if constexpr (SPLIT) {
@@ -598,10 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (fp32) and the two log-sums that weight it in the merge
             // (warp-uniform branches around the collective tcgen05.ld)
             if (!aborted) {
-                const bool mine = row < p.N && !*abort;
+                const bool mine = row < p.Nq && !*abort;
                 const bool any = T > 0 && l_all > 0.f;
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.N + (mine ? row : 0);
-                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.N;
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (mine ? row : 0);
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
                 if (mine) {
                     p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
                     p.lse_part[plane + i] = any ? m_ref * p.scale + logf(lhat_all) : -INFINITY;
@@ -636,10 +658,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
-                ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
-                ptx::tmem_wait_ld();
+                if (T > 0) {
+                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int u = 0; u < 32; ++u) ptx::reg_fence(ov[u]);
+                    for (int u = 0; u < 32; ++u) ptx::reg_fence(ov[u]);
+                } else {  // no key visible to this tile: O = 0 (U was never written)
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ov[u] = 0u;
+                }
                 // the Q tile's shared memory is free now (all S_x products are
                 // done) and becomes the staging buffer, in the 128-byte-swizzled
                 // layout the TMA store expects
@@ -667,13 +694,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!SPLIT && t == 0 && !*abort) {
 #pragma unroll
             for (int c = 0; c < C::kSub; ++c)
-                ptx::tma_store_3d(&tm_o, sQ(x) + c * kSubBytes, 64 * c, qb * kBlockM + x * kTileM, bh);
+                ptx::tma_store_4d(&tm_o, sQ(x) + c * kSubBytes, 64 * c, qb * kBlockM + x * kTileM,
+                                  h_idx, b_idx);
             ptx::bulk_commit_group();
             ptx::bulk_wait_group_read0();
         }
-        if (!SPLIT && !aborted && !*abort && row < p.N) {
+        if (!SPLIT && !aborted && !*abort && row < p.Nq) {
             const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
-            p.lse[static_cast<size_t>(bh) * p.N + row] = lse;
+            p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
         }
     }
 
@@ -690,15 +718,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 // normalised by the sum of its rounded weights, so w_s is that sum on the
 // common scale, which keeps O an exact convex combination of every weight
 // fed to P.V.  A warp per row; each lane owns d/32 consecutive columns.
+struct MergeParams {
+    const float* o_part;
+    const float* lse_part;
+    void* o;                            // row (b, h, i) at o + b o_sb + h o_sh + i o_sn
+    long long o_sb, o_sh, o_sn;
+    float* lse;                         // at lse + b lse_sb + h lse_sh + i
+    long long lse_sb, lse_sh;
+    int num_splits, H, Nq;
+    long long rows;                     // B H Nq
+};
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256)
-    fa_split_merge_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                          void* __restrict__ o, float* __restrict__ lse, int num_splits,
-                          long long rows) {
+__global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams mp) {
     constexpr int kPer = D / 32;
     const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    const long long rows = mp.rows;
+    const int num_splits = mp.num_splits;
+    const float* o_part = mp.o_part;
+    const float* lse_part = mp.lse_part;
     if (r >= rows) return;
+    const long long bh = r / mp.Nq, i = r % mp.Nq;
+    const long long b = bh / mp.H, h = bh % mp.H;
     const size_t plane = static_cast<size_t>(num_splits) * rows;
     float mh = -INFINITY, ml = -INFINITY;
     for (int s = 0; s < num_splits; ++s) {
@@ -727,10 +769,12 @@ __global__ void __launch_bounds__(256)
     uint32_t packed[kPer / 2];
 #pragma unroll
     for (int e = 0; e < kPer; e += 2) packed[e / 2] = pack2<BF16>(acc[e] * inv, acc[e + 1] * inv);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(o) + (r * D + lane * kPer) / 2;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(
+        static_cast<uint16_t*>(mp.o) + b * mp.o_sb + h * mp.o_sh + i * mp.o_sn + lane * kPer);
 #pragma unroll
     for (int e = 0; e < kPer / 2; ++e) dst[e] = packed[e];
-    if (lane == 0) lse[r] = (ml == -INFINITY) ? -INFINITY : ml + logf(lsum);
+    if (lane == 0)
+        mp.lse[b * mp.lse_sb + h * mp.lse_sh + i] = (ml == -INFINITY) ? -INFINITY : ml + logf(lsum);
 }
 
 }  // namespace fa

@@ -97,3 +97,29 @@ def test_splitkv_workspace_size_and_validation(lib):
     assert fa.fa_fwd_splitkv(*base, 4, ws, need - 1, None) == fa.FA_ERR_INVALID_ARG
     assert 1 <= fa.fa_splitkv_num_splits(1, 1, 4096, 64, 0) <= fa.FA_MAX_SPLITS
     assert fa.fa_splitkv_num_splits(64, 64, 4096, 128, 0) == 1
+
+
+def test_fa_fwd_ex_validation(lib):
+    a = fa.fa_fwd_args()
+    a.q, a.k, a.v, a.o, a.lse = A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000
+    a.B, a.H, a.Nq, a.Nk, a.d = 1, 2, 100, 300, 64
+    for f in ("q_stride", "k_stride", "v_stride", "o_stride"):
+        getattr(a, f)[:] = [2 * 300 * 64, 300 * 64, 64]
+    a.lse_stride[:] = [200, 100]
+    a.scale, a.mask, a.dtype, a.num_splits = 0.125, 3, fa.FA_FP16, 1
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG          # unknown mask
+    a.mask = fa.FA_MASK_CAUSAL_BOTTOM_RIGHT
+    a.k_stride[2] = 60                                        # not a multiple of 16 bytes
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_MISALIGNED
+    a.k_stride[2] = 64
+    a.o_stride[1] = 0
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_MISALIGNED
+    a.o_stride[1] = 300 * 64
+    a.Nk = 0
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG
+    a.Nk, a.lse_stride[1] = 300, 0
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG
+    a.lse_stride[1], a.d = 100, 80
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_UNSUPPORTED
+    a.d, a.num_splits, a.workspace = 64, 4, None
+    assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG          # split without a workspace
