@@ -41,9 +41,14 @@ sys.path.insert(0, ROOT)
 from online_softmax_tiling_gb300 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "T_b2h32n4096d128_bf16"
-KERNEL_SOURCES = ["online_softmax_tiling_gb300/csrc/fa_fwd_kernel.cuh",
-                  "online_softmax_tiling_gb300/csrc/sm103_ptx.cuh",
-                  "online_softmax_tiling_gb300/csrc/fa_api.cu"]
+_CSRC = "online_softmax_tiling_gb300/csrc/"
+# device code each timed path runs (the hash ties a committed ncu traffic
+# figure to the kernel source it was measured on)
+KERNEL_SOURCES = {
+    "fused": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh")],
+    "wide": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "fa_fwd_wide_kernel.cuh", "sm103_ptx.cuh")],
+    "naive": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "naive_attention.cuh", "sm103_ptx.cuh")],
+}
 METRIC = "attn fwd TFLOPS (4*B*H*N^2*d/t, causal halved) @N=4096; % of GB300 dense TC peak"
 
 
@@ -75,9 +80,9 @@ def barrier(world: int):
         dist.barrier()
 
 
-def kernel_hash() -> str:
+def kernel_hash(kind: str = "fused") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -170,6 +175,63 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+L2_BYTES = 129 * 10 ** 6
+
+
+def kernel_width(d: int) -> int:
+    """Width of the kernel that serves head dimension d (64, 128, 192 or 256)."""
+    return 64 if d <= 64 else 128 if d <= 128 else 192 if d <= 192 else 256
+
+
+def ceiling_counts(w: synth.Workload) -> dict:
+    """Per launch of the fused kernel: 2^x evaluations (one per visible query,
+    key pair) and bytes read from L2 into the SMs (each CTA's Q tile and the K
+    and V tiles it visits; tiles of 128 keys for d <= 128 with two 128-row
+    query tiles per CTA, 64 keys and one query tile per CTA above)."""
+    B, H, N, d = w.shape
+    wide = kernel_width(d) > 128
+    bm, bn = (128, 64) if wide else (256, 128)
+    nkv = -(-N // bn)
+    tiles = 0
+    for qb in range(-(-N // bm)):
+        if w.causal:
+            last = min(qb * bm + bm - 1, N - 1)
+            tiles += min(last // bn + 1, nkv)
+        else:
+            tiles += nkv
+    exps = B * H * (N * (N + 1) // 2 if w.causal else N * N)
+    l2 = B * H * (tiles * 2 * bn * d * 2 + N * d * 2)
+    return {"exps": exps, "l2_bytes": l2}
+
+
+def measure_ceilings(w, fa, torch, kernel_us: float, peaks: dict) -> dict:
+    """Rates of the exp unit and of L2 -> SM reads (microbenchmarks in the
+    library) turned into time floors for one launch of workload w."""
+    cnt = ceiling_counts(w)
+    buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    ex2 = fa.fa_ceiling_ex2_rate(torch.cuda.current_stream())
+    l2bw = fa.fa_ceiling_l2_read(buf.data_ptr(), buf.numel(), torch.cuda.current_stream())
+    del buf
+    return {
+        "ex2_per_s": round(ex2, -6), "l2_read_GBps": round(l2bw / 1e9, 1),
+        "per_launch": cnt,
+        "floors_us": {
+            "tensor": round(w.flops / (float(peaks.get("bf16_tflops", 1900.0)) * 1e12) * 1e6, 2),
+            "exp": round(cnt["exps"] / ex2 * 1e6, 2),
+            "l2_to_sm": round(cnt["l2_bytes"] / l2bw * 1e6, 2),
+            "hbm": round(w.compulsory_bytes / (float(peaks.get("hbm_gbs", 6800.0)) * 1e9) * 1e6, 2)},
+        "kernel_us": round(kernel_us, 2),
+    }
+
+
+def naive_model_bytes(w: synth.Workload) -> int:
+    """HBM bytes of the step-by-step computation as "CUDA 算子工程" 14.2 counts
+    them: Q, K, V read and O written once, S written once and read three
+    times, P written once and read once (16-bit elements)."""
+    B, H, N, d = w.shape
+    return B * H * (4 * N * d * 2 + 6 * N * N * 2)
+
+
 # -------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -199,15 +261,23 @@ def run_ours(args):
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
-    splits = args.num_splits
+    naive = args.path == "naive"
+    splits = 1 if naive else args.num_splits
     if splits == 0:
         splits = fa.fa_splitkv_num_splits(B, H, N, d, int(w.causal))
-    ws_bytes = fa.fa_splitkv_workspace_size(B, H, N, d, splits) if splits > 1 else 0
+    if naive:
+        ws_bytes = fa.fa_naive_workspace_size(B, H, N)
+    else:
+        ws_bytes = fa.fa_splitkv_workspace_size(B, H, N, d, splits) if splits > 1 else 0
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
-    launches_per_step = 2 if splits > 1 else 1
+    launches_per_step = 3 if naive else (2 if splits > 1 else 1)
 
     def step():
-        if splits > 1:
+        if naive:
+            st = fa.fa_naive_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, w.scale, int(w.causal), w.dtype,
+                                 ws.data_ptr(), ws_bytes, sptr)
+        elif splits > 1:
             st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                    lse.data_ptr(), B, H, N, d, w.scale, int(w.causal), w.dtype,
                                    splits, ws.data_ptr(), ws_bytes, sptr)
@@ -223,21 +293,35 @@ def run_ours(args):
     if fa.fa_check_device_status(sptr) != fa.FA_OK:
         raise RuntimeError("device status not OK after warm-up")
 
+    # inputs larger than L2 stream from HBM anyway; smaller ones get L2
+    # flushed (a 256 MiB fill, outside the timed launches) before every step
+    flush = w.compulsory_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush_buf.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
     torch.cuda.synchronize()
     wall_ms = (time.perf_counter() - t_wall) * 1e3
     barrier(world)
     clock_info = clocks.stop()
-    dev_ms = ev0.elapsed_time(ev1)
+    dev_ms = sum(a.elapsed_time(b) for a, b in evs) if flush else ev0.elapsed_time(ev1)
+    del flush_buf
     if fa.fa_check_device_status(sptr) != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed region")
     ms_total = max_over_ranks(dev_ms, world)
@@ -249,8 +333,24 @@ def run_ours(args):
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
     achieved = flops_rank / (dev_ms / args.steps * 1e-3) / 1e12
-    khash = kernel_hash()
-    traffic = profiled_traffic(args.workload, khash)
+    khash = kernel_hash("naive" if naive else ("wide" if kernel_width(d) > 128 else "fused"))
+    traffic = profiled_traffic(w.name + ("_naive" if naive else ""), khash)
+    if naive:
+        # the step-by-step baseline is bound by memory traffic: report the
+        # pages' byte count for it (S written, read three times, P written
+        # and read, Q, K, V, O once) against the measured HBM copy rate
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        model_bytes = naive_model_bytes(w)
+        gbs = model_bytes / (dev_ms / args.steps * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4), "traffic": traffic,
+                    "algorithmic_bytes": model_bytes,
+                    "peak_source": f"{peak_src} hbm_gbs", "kernel_hash": khash}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                    "kernel_hash": khash}
 
     # end-to-end through the public API with host buffers: H2D of q, k, v from
     # pinned memory, the fa_fwd call, D2H of O and LSE, every step
@@ -279,6 +379,10 @@ def run_ours(args):
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * 4
 
+    ceilings = None
+    if rank == 0 and not args.no_ceilings and not naive:
+        ceilings = measure_ceilings(w, fa, torch, dev_ms / args.steps * 1e3, peaks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
@@ -290,17 +394,18 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": synth.DTYPE_NAMES[w.dtype], "data": "synthetic (seeded N(0,1), SplitMix64 + Box-Muller)",
             "config": {**w.describe(), "parallelism": f"independent heads per rank x{world}",
-                       "num_splits": splits,
-                       "l2": "inputs larger than L2: 256 MiB of Q, K, V, O per step vs 129 MB L2",
+                       "num_splits": splits, "path": args.path,
+                       "l2": (f"L2 flushed before every step ({w.compulsory_bytes / 1e6:.1f} MB of "
+                              f"Q, K, V, O, LSE per step vs 129 MB L2)") if flush else
+                             (f"inputs larger than L2: {w.compulsory_bytes / 1e6:.1f} MB of Q, K, V, "
+                              f"O, LSE per step vs 129 MB L2"),
                        "pct_of_peak": round(100 * value / world / peak, 2)},
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "kernel_hash": khash},
+            "roofline": roofline,
             "e2e": {"value": round(flops_rank * world / (e2e_ms * 1e-3) / 1e12, 3),
                     "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * launches_per_step,
             "clocks": clock_info,
+            "ceilings": ceilings,
             "wall_ms_timed_region": round(wall_ms, 3),
             "cpu_baseline": cpu,
         }
@@ -388,6 +493,10 @@ def main(argv=None):
     ap.add_argument("--num-splits", type=int, default=1,
                     help="1 = one fused launch; 0 = library's split-KV choice; >= 2 = that many")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "naive"], default="fused",
+                    help="naive: the step-by-step baseline with S and P in HBM")
+    ap.add_argument("--no-ceilings", action="store_true",
+                    help="skip the exp-rate and L2-bandwidth microbenchmarks")
     ap.add_argument("--ref-rows", type=int, default=256)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -30,7 +30,8 @@ extern "C" {
 /* Status codes returned by every entry point. */
 #define FA_OK 0               /* success (for fa_fwd: validated and enqueued)            */
 #define FA_ERR_INVALID_ARG 1  /* null pointer, non-positive size, bad dtype, bad scale    */
-#define FA_ERR_UNSUPPORTED 2  /* valid request outside the compiled set (head dim d)      */
+#define FA_ERR_UNSUPPORTED 2  /* valid request outside the compiled set (head dim d), or a
+                                 split-KV request larger than the no-alloc scratch array   */
 #define FA_ERR_MISALIGNED 3   /* q, k, v or o not 16-byte aligned; lse not 4-byte aligned */
 #define FA_ERR_CUDA 4         /* a CUDA runtime/driver call failed (launch, encode, sync) */
 #define FA_ERR_TIMEOUT 5      /* a pipeline wait inside the kernel ran out of time        */
@@ -51,7 +52,11 @@ extern "C" {
  *           log-sum-exp of the scaled scores of each row.
  * B, H, N : batch, heads, sequence length (queries = keys = N); each >= 1.
  *           B*H and N must each fit the TMA tensor map (< 2^31).
- * d       : head dimension; 64 or 128 (anything else: FA_ERR_UNSUPPORTED).
+ * d       : head dimension: a multiple of 8 from 8 to 256 (else
+ *           FA_ERR_UNSUPPORTED).  64, 128, 192 and 256 run kernels of exactly
+ *           that width; any other d runs the next wider one, whose extra
+ *           columns are zero-filled on load and never stored (same result,
+ *           the time of the wider kernel).
  * scale   : the softmax scale s (for the standard definition 1/sqrt(d)); must
  *           be finite and > 0.  There is no default.
  * causal  : 0 = full attention, non-zero = key j visible to query i iff j <= i.
@@ -135,7 +140,8 @@ int fa_fwd_ex(const fa_fwd_args* args);
  * then about one wave of CTAs, with at least four key tiles per range. */
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal);
 
-/* Workspace bytes fa_fwd_splitkv needs for num_splits >= 2 (0 otherwise). */
+/* Workspace bytes fa_fwd_splitkv needs for num_splits >= 2 (0 otherwise, or
+ * for an unsupported d).  Partial O rows are as wide as the kernel serving d. */
 size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /*

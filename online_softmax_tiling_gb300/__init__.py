@@ -24,7 +24,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
 EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug",
            "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv",
-           "fa_fwd_splitkv_noalloc", "fa_fwd_ex")
+           "fa_fwd_splitkv_noalloc", "fa_fwd_ex", "fa_ceiling_ex2_rate", "fa_ceiling_l2_read",
+           "fa_naive_fwd", "fa_naive_workspace_size")
+FA_CEIL_OK, FA_CEIL_ERR_ARG, FA_CEIL_ERR_CUDA = 0, 1, 4
 FA_MASK_NONE, FA_MASK_CAUSAL_TOP_LEFT, FA_MASK_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 
 
@@ -87,6 +89,15 @@ def library() -> ctypes.CDLL:
             lib.fa_fwd_splitkv_noalloc.restype = i
             lib.fa_fwd_ex.argtypes = [ctypes.POINTER(fa_fwd_args)]
             lib.fa_fwd_ex.restype = i
+            lib.fa_ceiling_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+            lib.fa_ceiling_ex2_rate.restype = i
+            lib.fa_ceiling_l2_read.argtypes = [vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_double), vp]
+            lib.fa_ceiling_l2_read.restype = i
+            lib.fa_naive_workspace_size.argtypes = [i, i, i]
+            lib.fa_naive_workspace_size.restype = ctypes.c_size_t
+            lib.fa_naive_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, i, vp,
+                                         ctypes.c_size_t, vp]
+            lib.fa_naive_fwd.restype = i
             _lib = lib
         return _lib
 
@@ -132,6 +143,43 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, nu
 def fa_fwd_ex(args: "fa_fwd_args") -> int:
     """Raw C call of the general entry point with a filled `fa_fwd_args`."""
     return library().fa_fwd_ex(ctypes.byref(args))
+
+
+def fa_naive_workspace_size(B, H, N) -> int:
+    return library().fa_naive_workspace_size(int(B), int(H), int(N))
+
+
+def fa_naive_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, workspace, workspace_bytes,
+                 stream) -> int:
+    """Raw C call of the step-by-step baseline (include/fa_naive.h)."""
+    return library().fa_naive_fwd(q, k, v, o, lse, int(B), int(H), int(N), int(d), float(scale),
+                                  int(causal), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def _stream_handle(stream):
+    """A cudaStream_t address from None, an integer or a torch stream."""
+    if stream is None or isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def fa_ceiling_ex2_rate(stream=None) -> float:
+    """2^x evaluations per second on the current device (include/fa_ceilings.h)."""
+    out = ctypes.c_double()
+    st = library().fa_ceiling_ex2_rate(ctypes.byref(out), _stream_handle(stream))
+    if st != FA_CEIL_OK:
+        raise FaError(FA_ERR_CUDA, "fa_ceiling_ex2_rate")
+    return out.value
+
+
+def fa_ceiling_l2_read(buf, nbytes: int, stream=None) -> float:
+    """L2 -> SM read bytes per second over `nbytes` at device address `buf`."""
+    out = ctypes.c_double()
+    st = library().fa_ceiling_l2_read(buf, nbytes, ctypes.byref(out), _stream_handle(stream))
+    if st != FA_CEIL_OK:
+        raise FaError(FA_ERR_CUDA if st == FA_CEIL_ERR_CUDA else FA_ERR_INVALID_ARG,
+                      "fa_ceiling_l2_read")
+    return out.value
 
 
 def fa_check_device_status(stream=None) -> int:
@@ -250,4 +298,29 @@ def attention_forward_ex(q, k, v, scale: float | None = None, mask: int = FA_MAS
     st = fa_fwd_ex(a)
     if st != FA_OK:
         raise FaError(st, "fa_fwd_ex")
+    return out, lse
+
+
+def naive_attention_forward(q, k, v, scale: float | None = None, causal: bool = False, out=None,
+                            lse=None, workspace=None, stream=None):
+    """The step-by-step baseline for contiguous CUDA tensors [B, H, N, d]:
+    S and P are written to a workspace in HBM (allocated here unless given)."""
+    import torch
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    nbytes = fa_naive_workspace_size(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    st = fa_naive_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, H, N, d, scale, int(causal), _dtype_code(q), workspace.data_ptr(),
+                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_naive_fwd")
     return out, lse

@@ -1,4 +1,4 @@
-"""Build the sm_103a shared library in-tree with nvcc (no CMake, one translation unit)."""
+"""Build the sm_103a shared library in-tree with nvcc (no CMake, two translation units)."""
 from __future__ import annotations
 
 import os
@@ -8,9 +8,10 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = [os.path.join(CSRC, "fa_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh")] + [
-    os.path.join(ROOT, "include", "fa.h")]
+SOURCES = [os.path.join(CSRC, f) for f in ("fa_api.cu", "ceilings.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa_fwd_wide_kernel.cuh", "naive_attention.cuh",
+                                                     "sm103_ptx.cuh")] + [
+    os.path.join(ROOT, "include", f) for f in ("fa.h", "fa_ceilings.h", "fa_naive.h")]
 LIBRARY = os.path.join(HERE, "libfa_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -35,7 +36,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIBRARY
     tmp = LIBRARY + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-o", tmp, *SOURCES]
+           "--threads", "2", "-o", tmp, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)

@@ -14,9 +14,14 @@
 #include <cstdint>
 #include <algorithm>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "../../include/fa.h"
+#include "../../include/fa_naive.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_wide_kernel.cuh"
+#include "naive_attention.cuh"
 
 namespace {
 
@@ -42,10 +47,12 @@ EncodeTiledFn encode_fn() {
 // A 16-bit [B, H, rows, d] tensor with element strides (batch, head, row) and
 // contiguous d, viewed by TMA in 4-D (d, rows, H, B) so that rows >= `rows`
 // of one head are out of range (zero-filled on load, clipped on store)
-// instead of belonging to the next head.  Box: 64 columns (128 bytes, one
-// swizzle span) x 128 rows (one query tile or one key tile) x 1 x 1.
+// instead of belonging to the next head.  Columns >= d are out of range too:
+// a kernel wider than d reads zeros there and never writes them.  Box: 64
+// columns (128 bytes, one swizzle span) x box_rows rows (one query tile or
+// one key tile) x 1 x 1.
 bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t H, int64_t rows,
-               int64_t d, const long long (&stride)[3]) {
+               int64_t d, const long long (&stride)[3], uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
@@ -53,7 +60,7 @@ bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t 
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(stride[2]) * 2,
                                    static_cast<cuuint64_t>(stride[1]) * 2,
                                    static_cast<cuuint64_t>(stride[0]) * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {64, box_rows, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -62,15 +69,33 @@ bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Width of the kernel that serves head dimension d: 64, 128, 192 or 256,
+// the smallest that holds d (the columns beyond d are zeros: TMA fills them
+// on load and clips them on store); 0 = unsupported (d must be a multiple of
+// 8, a TMA stride rule, and at most 256).
+int kernel_dim(int d) {
+    if (d < 8 || d % 8 != 0 || d > 256) return 0;
+    return d <= 64 ? 64 : d <= 128 ? 128 : d <= 192 ? 192 : 256;
+}
+
 struct KernelEntry {
     const void* fn;
     int smem;
+    int threads;
+    int block_m;  // query rows per CTA
+    int block_n;  // keys per K/V tile (rows of the K and V boxes)
 };
 
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 KernelEntry entry() {
-    return KernelEntry{reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>),
-                       fa::Cfg<D>::kSmemBytes};
+    if constexpr (D <= 128)
+        return KernelEntry{
+            reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>),
+            fa::Cfg<D>::kSmemBytes, fa::kThreads, fa::kBlockM, fa::kBlockN};
+    else
+        return KernelEntry{
+            reinterpret_cast<const void*>(&fa::fa_fwd_wide_kernel<D, BF16, CAUSAL, SPLIT>),
+            fa::WideCfg<D>::kSmemBytes, fa::kWideThreads, fa::kTileM, fa::kWideBlockN};
 }
 
 template <int D, bool BF16>
@@ -79,43 +104,47 @@ KernelEntry select_d_dtype(bool causal, bool split) {
     return split ? entry<D, BF16, false, true>() : entry<D, BF16, false, false>();
 }
 
-KernelEntry select_kernel(int d, int dtype, bool causal, bool split) {
+// kd: a kernel width from kernel_dim()
+KernelEntry select_kernel(int kd, int dtype, bool causal, bool split) {
     const bool bf = dtype == FA_BF16;
-    if (d == 64) return bf ? select_d_dtype<64, true>(causal, split) : select_d_dtype<64, false>(causal, split);
-    return bf ? select_d_dtype<128, true>(causal, split) : select_d_dtype<128, false>(causal, split);
+    switch (kd) {
+        case 64: return bf ? select_d_dtype<64, true>(causal, split) : select_d_dtype<64, false>(causal, split);
+        case 128: return bf ? select_d_dtype<128, true>(causal, split) : select_d_dtype<128, false>(causal, split);
+        case 192: return bf ? select_d_dtype<192, true>(causal, split) : select_d_dtype<192, false>(causal, split);
+        default: return bf ? select_d_dtype<256, true>(causal, split) : select_d_dtype<256, false>(causal, split);
+    }
 }
 
-const void* select_merge(int d, int dtype) {
+template <int D>
+const void* merge_fn(bool bf) {
+    return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, true>)
+              : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, false>);
+}
+
+const void* select_merge(int kd, int dtype) {
     const bool bf = dtype == FA_BF16;
-    if (d == 64)
-        return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<64, true>)
-                  : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<64, false>);
-    return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<128, true>)
-              : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<128, false>);
+    switch (kd) {
+        case 64: return merge_fn<64>(bf);
+        case 128: return merge_fn<128>(bf);
+        case 192: return merge_fn<192>(bf);
+        default: return merge_fn<256>(bf);
+    }
 }
 
 // Opt each kernel into its dynamic shared memory once per device.
 bool ensure_smem_attr(const void* fn, int smem, int device) {
     static std::mutex mu;
-    static std::atomic<uint64_t> done_mask[16][64];  // [kernel slot][device / 64 word]
-    static const void* slots[16] = {};
+    static std::set<std::pair<const void*, int>> done;  // (kernel, device) already set
     std::lock_guard<std::mutex> lock(mu);
-    int slot = -1;
-    for (int i = 0; i < 16; ++i) {
-        if (slots[i] == fn) { slot = i; break; }
-        if (slots[i] == nullptr) { slots[i] = fn; slot = i; break; }
-    }
-    if (slot < 0 || device < 0 || device >= 64 * 64) return false;
-    const uint64_t bit = 1ull << (device & 63);
-    if (done_mask[slot][device >> 6].load() & bit) return true;
+    if (done.count({fn, device})) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return false;
-    done_mask[slot][device >> 6].fetch_or(bit);
+    done.insert({fn, device});
     return true;
 }
 
-// Workspace layout of split-KV: o_part [S][BH][N][d] fp32, then (256-byte
-// aligned) lse_part [2][S][BH][N] fp32.
+// Workspace layout of split-KV: o_part [S][BH][N][kd] fp32 (kd the kernel
+// width), then (256-byte aligned) lse_part [2][S][BH][N] fp32.
 size_t split_o_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
     return (static_cast<size_t>(S * BH * N * d) * 4 + 255) & ~static_cast<size_t>(255);
 }
@@ -154,9 +183,12 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         return FA_ERR_INVALID_ARG;
     if (!(timeout_s > 0.0) || !std::isfinite(timeout_s)) return FA_ERR_INVALID_ARG;
     if (fault_mode < 0 || fault_mode > 1) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int kd = kernel_dim(d);
+    if (kd == 0) return FA_ERR_UNSUPPORTED;
+    const bool causal = a.mask != FA_MASK_NONE;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    const int64_t nq = (static_cast<int64_t>(Nq) + fa::kBlockM - 1) / fa::kBlockM;  // CTAs per head
+    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // CTAs per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
     // TMA: every stride a positive multiple of 16 bytes (8 16-bit elements);
     // LSE rows contiguous, its strides positive
@@ -178,21 +210,22 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     if (split) {
         if (!a.workspace) return FA_ERR_INVALID_ARG;
         if (misaligned(a.workspace, 256)) return FA_ERR_MISALIGNED;
-        if (a.workspace_bytes < split_workspace_bytes(num_splits, BH, Nq, d)) return FA_ERR_INVALID_ARG;
+        if (a.workspace_bytes < split_workspace_bytes(num_splits, BH, Nq, kd)) return FA_ERR_INVALID_ARG;
         if (BH * nq * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
     }
 
+    const KernelEntry ke = select_kernel(kd, dtype, causal, split);
+    const uint32_t qrows = static_cast<uint32_t>(fa::kTileM);
+    const uint32_t krows = static_cast<uint32_t>(ke.block_n);
     CUtensorMap tq, tk, tv, to;
-    if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride) ||
-        !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride) ||
-        !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride) ||
-        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride))
+    if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride, qrows) ||
+        !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride, krows) ||
+        !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride, krows) ||
+        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, qrows))
         return FA_ERR_CUDA;
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
-    const bool causal = a.mask != FA_MASK_NONE;
-    const KernelEntry ke = select_kernel(d, dtype, causal, split);
     if (!ensure_smem_attr(ke.fn, ke.smem, device)) return FA_ERR_CUDA;
 
     fa::FwdParams prm;
@@ -212,12 +245,12 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     prm.BH = static_cast<int>(BH);
     prm.o_part = split ? static_cast<float*>(a.workspace) : nullptr;
     prm.lse_part = split ? reinterpret_cast<float*>(static_cast<char*>(a.workspace) +
-                                                    split_o_bytes(num_splits, BH, Nq, d))
+                                                    split_o_bytes(num_splits, BH, Nq, kd))
                          : nullptr;
 
     void* args[] = {&tq, &tk, &tv, &to, &prm};
     const dim3 grid(static_cast<unsigned>(BH * nq * num_splits));
-    const dim3 block(fa::kThreads);
+    const dim3 block(static_cast<unsigned>(ke.threads));
     const cudaStream_t st = static_cast<cudaStream_t>(a.stream);
     if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem), st) != cudaSuccess)
         return FA_ERR_CUDA;
@@ -235,10 +268,11 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         mp.num_splits = num_splits;
         mp.H = H;
         mp.Nq = Nq;
+        mp.d_out = d;
         mp.rows = BH * Nq;
         void* margs[] = {&mp};
         const dim3 mgrid(static_cast<unsigned>((mp.rows + 7) / 8));
-        if (cudaLaunchKernel(select_merge(d, dtype), mgrid, dim3(256), margs, 0, st) != cudaSuccess)
+        if (cudaLaunchKernel(select_merge(kd, dtype), mgrid, dim3(256), margs, 0, st) != cudaSuccess)
             return FA_ERR_CUDA;
     }
     return FA_OK;
@@ -268,26 +302,28 @@ int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* ls
 
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
     (void)causal;
-    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 1;
+    const int kd = kernel_dim(d);
+    if (B < 1 || H < 1 || N < 1 || kd == 0) return 1;
     int device = 0, sms = 148;
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         sms = 148;
     // Splitting pays for its fp32 partials and merge only when most SMs would
     // otherwise idle: split when the blocks fill less than half of them, into
-    // about one wave, keeping at least four key tiles per range.
-    const int64_t ctas = static_cast<int64_t>(B) * H * ((N + fa::kBlockM - 1) / fa::kBlockM);
+    // about one wave, keeping at least 512 keys per range.
+    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t ctas = static_cast<int64_t>(B) * H * ((N + block_m - 1) / block_m);
     if (2 * ctas > sms) return 1;
-    const int64_t nkv = (static_cast<int64_t>(N) + fa::kBlockN - 1) / fa::kBlockN;
     int64_t s = (static_cast<int64_t>(sms) + ctas - 1) / ctas;
-    s = std::min<int64_t>(s, std::max<int64_t>(1, nkv / 4));
+    s = std::min<int64_t>(s, std::max<int64_t>(1, static_cast<int64_t>(N) / 512));
     s = std::min<int64_t>(s, FA_MAX_SPLITS);
     return static_cast<int>(std::max<int64_t>(1, s));
 }
 
 size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
-    if (B < 1 || H < 1 || N < 1 || d < 1 || num_splits < 2) return 0;
-    return split_workspace_bytes(num_splits, static_cast<int64_t>(B) * H, N, d);
+    const int kd = kernel_dim(d);
+    if (B < 1 || H < 1 || N < 1 || kd == 0 || num_splits < 2) return 0;
+    return split_workspace_bytes(num_splits, static_cast<int64_t>(B) * H, N, kd);
 }
 
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -371,5 +407,108 @@ const char* fa_status_string(int status) {
 }
 
 int fa_version(void) { return 100; }
+
+}  // extern "C"
+
+// ---- the step-by-step baseline (S and P in HBM) ---------------------------
+namespace {
+
+size_t naive_matrix_bytes(int64_t BH, int64_t N) {
+    return (static_cast<size_t>(BH * N * N) * 2 + 255) & ~static_cast<size_t>(255);
+}
+
+template <int D, bool BF16>
+int naive_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const CUtensorMap& to, const CUtensorMap& ts, const CUtensorMap& tp,
+                 const uint16_t* S, uint16_t* P, float* lse, int H, int64_t BH, int N,
+                 float scale, int causal, cudaStream_t st) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
+    const unsigned long long tmo = 2000000000ull;
+    const void* f1 = reinterpret_cast<const void*>(&fa::fa_naive_scores_kernel<D, BF16>);
+    const void* f2 = reinterpret_cast<const void*>(&fa::fa_naive_softmax_kernel<BF16>);
+    const void* f3 = reinterpret_cast<const void*>(&fa::fa_naive_pv_kernel<D, BF16>);
+    const int sm1 = fa::NaiveScoresCfg<D>::kSmemBytes, sm3 = fa::NaivePvCfg<D>::kSmemBytes;
+    if (!ensure_smem_attr(f1, sm1, device) || !ensure_smem_attr(f3, sm3, device)) return FA_ERR_CUDA;
+    const unsigned nt = static_cast<unsigned>((N + 127) / 128);
+    {
+        int h = H;
+        float sc = scale;
+        unsigned long long t = tmo;
+        void* args[] = {const_cast<CUtensorMap*>(&tq), const_cast<CUtensorMap*>(&tk),
+                        const_cast<CUtensorMap*>(&ts), &h, &sc, &t};
+        if (cudaLaunchKernel(f1, dim3(nt, nt, static_cast<unsigned>(BH)), dim3(fa::kNaiveThreads),
+                             args, sm1, st) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    {
+        const uint16_t* s_ = S;
+        uint16_t* p_ = P;
+        float* l_ = lse;
+        int n = N, c = causal, off = 0;
+        void* args[] = {&s_, &p_, &l_, &n, &c, &off};
+        if (cudaLaunchKernel(f2, dim3(static_cast<unsigned>(BH * N)), dim3(fa::kNaiveSoftmaxThreads),
+                             args, 0, st) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    {
+        int h = H, n = N;
+        unsigned long long t = tmo;
+        void* args[] = {const_cast<CUtensorMap*>(&tp), const_cast<CUtensorMap*>(&tv),
+                        const_cast<CUtensorMap*>(&to), &h, &n, &t};
+        if (cudaLaunchKernel(f3, dim3(nt, static_cast<unsigned>(BH)), dim3(fa::kNaivePvThreads),
+                             args, sm3, st) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_naive_workspace_size(int B, int H, int N) {
+    if (B < 1 || H < 1 || N < 1) return 0;
+    return 2 * naive_matrix_bytes(static_cast<int64_t>(B) * H, N);
+}
+
+int fa_naive_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, int dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (N % 8 != 0) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (BH > 65535 || (N + 127) / 128 > 65535 || BH * N > INT32_MAX) return FA_ERR_INVALID_ARG;
+    auto misaligned = [](const void* ptr, uintptr_t al) {
+        return (reinterpret_cast<uintptr_t>(ptr) & (al - 1)) != 0;
+    };
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
+        misaligned(lse, 4) || misaligned(workspace, 256))
+        return FA_ERR_MISALIGNED;
+    if (workspace_bytes < fa_naive_workspace_size(B, H, N)) return FA_ERR_INVALID_ARG;
+    uint16_t* S = static_cast<uint16_t*>(workspace);
+    uint16_t* P = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + naive_matrix_bytes(BH, N));
+    fa_fwd_args a = contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
+    const long long mat[3] = {BH * N * N, static_cast<long long>(N) * N, N};
+    CUtensorMap tq, tk, tv, to, ts, tp;
+    if (!encode_4d(&tq, q, dtype, B, H, N, d, a.q_stride, 128) ||
+        !encode_4d(&tk, k, dtype, B, H, N, d, a.k_stride, 128) ||
+        !encode_4d(&tv, v, dtype, B, H, N, d, a.v_stride, 128) ||
+        !encode_4d(&to, o, dtype, B, H, N, d, a.o_stride, 128) ||
+        !encode_4d(&ts, S, dtype, 1, BH, N, N, mat, 128) ||
+        !encode_4d(&tp, P, dtype, 1, BH, N, N, mat, 128))
+        return FA_ERR_CUDA;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool bf = dtype == FA_BF16;
+    if (d == 64)
+        return bf ? naive_launch<64, true>(tq, tk, tv, to, ts, tp, S, P, lse, H, BH, N, scale, causal, st)
+                  : naive_launch<64, false>(tq, tk, tv, to, ts, tp, S, P, lse, H, BH, N, scale, causal, st);
+    return bf ? naive_launch<128, true>(tq, tk, tv, to, ts, tp, S, P, lse, H, BH, N, scale, causal, st)
+              : naive_launch<128, false>(tq, tk, tv, to, ts, tp, S, P, lse, H, BH, N, scale, causal, st);
+}
 
 }  // extern "C"

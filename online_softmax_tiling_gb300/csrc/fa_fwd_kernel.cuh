@@ -717,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // O = sum_s w_s O_s / sum_s w_s with w_s = e^{LSEhat_s - max}: O_s is
 // normalised by the sum of its rounded weights, so w_s is that sum on the
 // common scale, which keeps O an exact convex combination of every weight
-// fed to P.V.  A warp per row; each lane owns d/32 consecutive columns.
+// fed to P.V.  A warp per row; each lane owns D/32 consecutive columns of the
+// kernel's width D, of which the first d_out are written.
 struct MergeParams {
     const float* o_part;
     const float* lse_part;
@@ -726,6 +727,7 @@ struct MergeParams {
     float* lse;                         // at lse + b lse_sb + h lse_sh + i
     long long lse_sb, lse_sh;
     int num_splits, H, Nq;
+    int d_out;                          // columns of O written (<= D, a multiple of 8)
     long long rows;                     // B H Nq
 };
 
@@ -772,7 +774,8 @@ __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams m
     uint32_t* dst = reinterpret_cast<uint32_t*>(
         static_cast<uint16_t*>(mp.o) + b * mp.o_sb + h * mp.o_sh + i * mp.o_sn + lane * kPer);
 #pragma unroll
-    for (int e = 0; e < kPer / 2; ++e) dst[e] = packed[e];
+    for (int e = 0; e < kPer / 2; ++e)
+        if (lane * kPer + 2 * e < mp.d_out) dst[e] = packed[e];
     if (lane == 0)
         mp.lse[b * mp.lse_sb + h * mp.lse_sh + i] = (ml == -INFINITY) ? -INFINITY : ml + logf(lsum);
 }

@@ -1,0 +1,530 @@
+// fa_fwd_wide_kernel.cuh - the same fused attention forward for head
+// dimensions 192 and 256 on sm_103a.
+//
+// It computes exactly what fa_fwd_kernel computes (the online softmax of
+// "用 CuTe 读懂 FlashAttention：一次 forward 的完整流程", sections "第四步",
+// "第五步" and "最后", in the FlashAttention-2 loop order of "CUDA 算子工程"
+// ch. 14, section 14.5), with the same reference-first weights, the same two
+// weight sums, masks, split-KV partials and bounded waits.  What changes is
+// the tiling, because a wide head does not fit the two-query-tile layout:
+// two tiles would need 2 x (128 + d) TMEM columns, more than the 512 an SM has.
+//
+//   * one CTA per 128-row query tile; 6 warps: warps 0-3 softmax + epilogue
+//     (thread t owns row t = TMEM lane t), warp 4 the TMA loader, warp 5 the
+//     tensor-core issuer;
+//   * key tiles of 64 keys (K and V tiles of 64 x d, 2-3 stages each);
+//   * TMEM: two score buffers S0 at column 0 and S1 at 64 (64 fp32 columns;
+//     the weights P overwrite the first 32), U at column 128 (d columns);
+//   * tensor-core order: S(0), S(1), then per key tile j: PV(j), S(j+2).
+//     The softmax of tile j+1 runs while the tensor core computes PV(j) and
+//     S(j+2) - with d = 256 each is 512 cycles, so the softmax of 64 keys
+//     (about half that) stays off the critical path.
+//   * S(j+1) is issued before PV(j), so U may still be absorbing P(j-1) V
+//     when the softmax of tile j wants to rescale it: that (rare) rescale
+//     first waits for PV(j-1).  Each score buffer has its own "weights
+//     written" barrier, because the softmax can run one tile ahead of the
+//     issuer's wait; and "U has absorbed P(j) V" alternates between two
+//     barriers by the parity of j: when a softmax warp finishes its last
+//     tile n-1, PV(n-3) is certain to be complete but PV(n-2) is not, so a
+//     single barrier could be two phases behind the one awaited, and a
+//     parity wait cannot tell two phases apart.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+constexpr int kWideBlockN = 64;      // keys per tile
+constexpr int kWideThreads = 192;    // 4 softmax warps + loader warp + MMA warp
+constexpr int kWideLoaderWarp = 4;
+constexpr int kWideMmaWarp = 5;
+constexpr uint32_t kWideTmemU = 128;  // S0 at 0, S1 at 64, U at 128
+
+template <int D>
+struct WideCfg {
+    static_assert(D == 192 || D == 256, "wide head dim");
+    static constexpr int kSub = D / 64;                      // 64-column swizzle sub-tiles
+    static constexpr int kQSubBytes = kTileM * 128;          // 128 rows x 128 bytes
+    static constexpr int kKVSubBytes = kWideBlockN * 128;    // 64 rows x 128 bytes
+    static constexpr int kQBytes = kSub * kQSubBytes;
+    static constexpr int kKVBytes = kSub * kKVSubBytes;
+    static constexpr int kKStages = D == 256 ? 2 : 3;
+    static constexpr int kVStages = D == 256 ? 2 : 3;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kQBytes;
+    static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+    static constexpr int kOffCtl = kOffV + kVStages * kKVBytes;
+    static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
+};
+
+template <int NK, int NV>
+struct alignas(8) WideCtl {
+    uint64_t q_full;
+    uint64_t k_full[NK];
+    uint64_t k_empty[NK];
+    uint64_t v_full[NV];
+    uint64_t v_empty[NV];
+    uint64_t s_full[2];  // per score buffer: S(j) is in TMEM
+    uint64_t p_full[2];  // per score buffer: P(j) is in TMEM (and U rescaled)
+    uint64_t o_ready[2];  // by the parity of j: U has absorbed P(j) V_j
+    uint64_t drain;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    fa_fwd_wide_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+    using C = WideCfg<D>;
+    constexpr int NK = C::kKStages;
+    constexpr int NV = C::kVStages;
+    constexpr int BN = kWideBlockN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = ptx::smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = ptx::smem_addr(smem);
+    WideCtl<NK, NV>* ctl = reinterpret_cast<WideCtl<NK, NV>*>(smem + C::kOffCtl);
+    volatile uint32_t* abort = &ctl->abort;
+    const unsigned long long tmo = p.timeout_ns;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // ---- which rows (one 128-row tile per CTA; longest causal tiles first)
+    const int split = SPLIT ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
+    const int blk = SPLIT ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
+    const int bh = blk / p.num_q_blocks;
+    int qb = blk % p.num_q_blocks;
+    if (CAUSAL) qb = p.num_q_blocks - 1 - qb;
+    const int b_idx = bh / p.H, h_idx = bh % p.H;
+    const int first_row = qb * kTileM;
+    const int nkv = (p.Nk + BN - 1) / BN;
+    int T = nkv;  // key tiles visible to the tile
+    if (CAUSAL) {
+        const int last = min(first_row + kTileM - 1, p.Nq - 1) + p.mask_offset;
+        T = last < 0 ? 0 : min(last / BN + 1, nkv);
+    }
+    int k0 = 0, n = T;  // this CTA visits key tiles k0 .. k0 + n - 1
+    if constexpr (SPLIT) {
+        const int chunk = (T + p.num_splits - 1) / p.num_splits;
+        k0 = split * chunk;
+        n = max(0, min(k0 + chunk, T) - k0);
+        if (n == 0) {  // empty range: its partials carry no weight
+            const int row = first_row + static_cast<int>(threadIdx.x);
+            if (threadIdx.x < kTileM && row < p.Nq) {
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
+                p.lse_part[i] = -INFINITY;
+                p.lse_part[plane + i] = -INFINITY;
+            }
+            return;
+        }
+    }
+
+    const uint32_t bar_q = ptx::smem_addr(&ctl->q_full);
+    auto bar_kf = [&](int s) { return ptx::smem_addr(&ctl->k_full[s]); };
+    auto bar_ke = [&](int s) { return ptx::smem_addr(&ctl->k_empty[s]); };
+    auto bar_vf = [&](int s) { return ptx::smem_addr(&ctl->v_full[s]); };
+    auto bar_ve = [&](int s) { return ptx::smem_addr(&ctl->v_empty[s]); };
+    auto bar_sf = [&](int b) { return ptx::smem_addr(&ctl->s_full[b]); };
+    auto bar_pf = [&](int b) { return ptx::smem_addr(&ctl->p_full[b]); };
+    auto bar_o = [&](int j) { return ptx::smem_addr(&ctl->o_ready[j & 1]); };
+    const uint32_t bar_drain = ptx::smem_addr(&ctl->drain);
+    const uint32_t sQ = sbase + C::kOffQ;
+    auto sK = [&](int s) { return sbase + C::kOffK + s * C::kKVBytes; };
+    auto sV = [&](int s) { return sbase + C::kOffV + s * C::kKVBytes; };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_q, 1);
+        for (int s = 0; s < NK; ++s) {
+            ptx::mbar_init(bar_kf(s), 1);
+            ptx::mbar_init(bar_ke(s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            ptx::mbar_init(bar_vf(s), 1);
+            ptx::mbar_init(bar_ve(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_sf(b), 1);
+            ptx::mbar_init(bar_pf(b), kTileM);
+        }
+        ptx::mbar_init(bar_o(0), 1);
+        ptx::mbar_init(bar_o(1), 1);
+        ptx::mbar_init(bar_drain, 1);
+        ctl->abort = 0u;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kWideLoaderWarp && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_o);
+    }
+    if (warp == kWideMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == kWideLoaderWarp) {
+        // =============================================================== loader
+        // Q once; then K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V.
+        int issued_k[NK], issued_v[NV];
+#pragma unroll
+        for (int s = 0; s < NK; ++s) issued_k[s] = 0;
+#pragma unroll
+        for (int s = 0; s < NV; ++s) issued_v[s] = 0;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar_q, C::kQBytes);
+#pragma unroll
+            for (int c = 0; c < C::kSub; ++c)
+                ptx::tma_load_4d(sQ + c * C::kQSubBytes, &tm_q, bar_q, 64 * c, first_row, h_idx,
+                                 b_idx);
+        }
+        for (int j = 0; j <= n; ++j) {
+            if (j < n) {
+                const int s = j % NK;
+                if (j >= NK && !wait_warp(bar_ke(s), ((j / NK) - 1) & 1, abort, tmo)) break;
+                const bool skip = (p.fault_mode == 1 && j == 0);
+                if (lane == 0 && !skip) {
+                    ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kSub; ++c)
+                        ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
+                                         (k0 + j) * BN, h_idx, b_idx);
+                }
+                if (!skip) ++issued_k[s];
+            }
+            if (j >= 1) {
+                const int jv = j - 1;
+                const int s = jv % NV;
+                if (jv >= NV && !wait_warp(bar_ve(s), ((jv / NV) - 1) & 1, abort, tmo)) break;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
+#pragma unroll
+                    for (int c = 0; c < C::kSub; ++c)
+                        ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
+                                         (k0 + jv) * BN, h_idx, b_idx);
+                }
+                ++issued_v[s];
+            }
+        }
+        // Never leave the CTA with copies still landing in its shared memory.
+        wait_warp(bar_q, 0, abort, tmo, false);
+        for (int s = 0; s < NK; ++s)
+            if (issued_k[s] > 0) wait_warp(bar_kf(s), (issued_k[s] - 1) & 1, abort, tmo, false);
+        for (int s = 0; s < NV; ++s)
+            if (issued_v[s] > 0) wait_warp(bar_vf(s), (issued_v[s] - 1) & 1, abort, tmo, false);
+    } else if (warp == kWideMmaWarp) {
+        // ====================================================== tensor-core issuer
+        constexpr uint32_t idesc_s = instr_desc(BF16, kTileM, BN, false);
+        constexpr uint32_t idesc_pv = instr_desc(BF16, kTileM, D, true);
+        const uint64_t q_desc = smem_desc(sQ, 16, 1024);
+        const uint64_t k_desc0 = smem_desc(sK(0), 16, 1024);
+        // V is MN-major: the next 64 columns of d are one sub-tile further on
+        const uint64_t v_desc0 = smem_desc(sV(0), C::kKVSubBytes, 1024);
+        constexpr uint64_t kStageStep = C::kKVBytes / 16;
+        // S_b = Q K_s^T: d/16 steps of K16; +32 bytes per step inside a
+        // 128-byte swizzle row, the next 64-column sub-tile after four steps
+        auto issue_s = [&](int b, int s) {
+            if (ptx::elect_one()) {
+                const uint64_t kd = k_desc0 + s * kStageStep;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t ao = (k >> 2) * (C::kQSubBytes / 16) + (k & 3) * 2;
+                    const uint64_t bo = (k >> 2) * (C::kKVSubBytes / 16) + (k & 3) * 2;
+                    ptx::mma_ss(tmem + b * BN, q_desc + ao, kd + bo, idesc_s, k > 0 ? 1u : 0u);
+                }
+            }
+            __syncwarp();
+        };
+        // U (+)= P_b V_s: 64 keys = 4 steps of K16; P advances 8 TMEM columns
+        // (16 packed 16-bit weights), V 16 rows = 2048 bytes per step
+        auto issue_pv = [&](int b, int s, bool acc) {
+            if (ptx::elect_one()) {
+                const uint64_t vd = v_desc0 + s * kStageStep;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    ptx::mma_ts(tmem + kWideTmemU, tmem + b * BN + k * 8, vd + k * 128, idesc_pv,
+                                (acc || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+        };
+        bool ok = n > 0 && wait_warp(bar_q, 0, abort, tmo);
+        for (int j = 0; ok && j < 2 && j < n; ++j) {
+            if (!(ok = wait_warp(bar_kf(j % NK), (j / NK) & 1, abort, tmo))) break;
+            ptx::tc_fence_after_sync();
+            issue_s(j, j % NK);
+            ptx::tc_commit_elect(bar_sf(j));
+            ptx::tc_commit_elect(bar_ke(j % NK));
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < n; ++j) {
+            const int b = j & 1;
+            const int sv = j % NV;
+            if (!(ok = wait_warp(bar_vf(sv), (j / NV) & 1, abort, tmo))) break;
+            if (!(ok = wait_warp(bar_pf(b), (j >> 1) & 1, abort, tmo))) break;
+            ptx::tc_fence_after_sync();
+            issue_pv(b, sv, j > 0);
+            ptx::tc_commit_elect(bar_o(j));
+            ptx::tc_commit_elect(bar_ve(sv));
+            __syncwarp();
+            if (j + 2 < n) {
+                const int sk = (j + 2) % NK;
+                if (!(ok = wait_warp(bar_kf(sk), ((j + 2) / NK) & 1, abort, tmo))) break;
+                ptx::tc_fence_after_sync();
+                issue_s(b, sk);  // into the buffer PV(j) has just read (issued in order)
+                ptx::tc_commit_elect(bar_sf(b));
+                ptx::tc_commit_elect(bar_ke(sk));
+                __syncwarp();
+            }
+        }
+        // Drain: nothing of ours may still run on the tensor core at teardown.
+        ptx::tc_commit_elect(bar_drain);
+        __syncwarp();
+        wait_warp(bar_drain, 0, abort, tmo, false);
+    } else {
+        // ======================================== softmax + epilogue (warps 0-3)
+        const int t = threadIdx.x;                    // row in the tile = TMEM lane
+        const int row = first_row + t;                // query index in the head
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t u_addr = tmem + lane_off + kWideTmemU;
+        const float c2 = p.scale_log2;
+        const float2 c2v = make_float2(c2, c2);
+        auto tile_masked = [&](int j) {
+            const int kend = (k0 + j + 1) * BN;
+            return kend > p.Nk || (CAUSAL && kend - 1 > first_row + p.mask_offset);
+        };
+        auto key_limit = [&](int kbase) {
+            int limit = p.Nk - kbase;
+            if (CAUSAL) limit = min(limit, row + p.mask_offset - kbase + 1);
+            return limit;
+        };
+        // scores [32 c, 32 c + 32) of tile j (buffer at s_addr), masked to -inf
+        // where this row may not see the key
+        auto load_chunk = [&](uint32_t s_addr, uint32_t(&sv)[32], int c, int j) {
+            ptx::tmem_ld_32x32b_x32(s_addr + c * 32, sv);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) ptx::reg_fence(sv[u]);
+            if (tile_masked(j)) {
+                const int limit = key_limit((k0 + j) * BN + c * 32);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    if (u >= limit) sv[u] = __float_as_uint(-INFINITY);
+            }
+        };
+        auto weights = [&](const uint32_t* sv, int npairs, float neg_ref, uint32_t* pk,
+                           float2 (&rs)[2], float2 (&rh)[2]) {
+            const float2 nrv = make_float2(neg_ref, neg_ref);
+#pragma unroll
+            for (int c = 0; c < npairs; ++c) {
+                const float2 e = __ffma2_rn(
+                    make_float2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2v, nrv);
+                const float2 pw = make_float2(ptx::ex2_approx(e.x), ptx::ex2_approx(e.y));
+                rs[c & 1] = __fadd2_rn(rs[c & 1], pw);
+                pk[c] = pack2<BF16>(pw.x, pw.y);
+                add_packed<BF16>(rh[c & 1], pk[c]);
+            }
+        };
+        float m_ref = -INFINITY;
+        float2 lsum = make_float2(0.f, 0.f);
+        float2 lhat = make_float2(0.f, 0.f);
+        bool aborted = false;
+
+        for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            if (!wait_warp(bar_sf(b), (j >> 1) & 1, abort, tmo)) {
+                aborted = true;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const uint32_t s_addr = tmem + lane_off + b * BN;
+            uint32_t pk[BN / 2];
+            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            // (tcgen05.ld is warp-collective: every branch around it is uniform)
+            bool redo = (m_ref == -INFINITY);
+            if (!__any_sync(0xffffffffu, redo)) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t sv[32];
+                    load_chunk(s_addr, sv, c, j);
+                    weights(sv, 16, -m_ref * c2, &pk[16 * c], rs, rh);
+                }
+                redo = rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
+            }
+            float alpha = 1.f;
+            float m_new = m_ref;
+            if (__any_sync(0xffffffffu, redo)) {
+                float mt = -INFINITY;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t sv[32];
+                    load_chunk(s_addr, sv, c, j);
+                    float mx[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
+#pragma unroll
+                    for (int u = 4; u + 8 <= 32; u += 8)
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
+                                               __uint_as_float(sv[u + 4 + w]));
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
+                    mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                }
+                if (redo) {
+                    m_new = fmaxf(mt, m_ref);
+                    if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                }
+                const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
+                rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t sv[32];
+                    load_chunk(s_addr, sv, c, j);
+                    weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
+                }
+            }
+            const float2 av = make_float2(alpha, alpha);
+            const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
+            lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
+            lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
+            ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+            // U may still be absorbing P(j-1) V (issued after S(j)): a rescale
+            // waits for that product first (warp-uniform)
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (j > 0 && !wait_warp(bar_o(j - 1), ((j - 1) >> 1) & 1, abort, tmo)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+#pragma unroll 1
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t ov[16];
+                    ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 16; u += 2) {
+                        ptx::reg_fence(ov[u]);
+                        ptx::reg_fence(ov[u + 1]);
+                        const float2 rr = __fmul2_rn(
+                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), av);
+                        ov[u] = __float_as_uint(rr.x);
+                        ov[u + 1] = __float_as_uint(rr.y);
+                    }
+                    ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(bar_pf(b));
+            m_ref = m_new;
+        }
+
+        // ---- epilogue: O = U / lhat -> 16-bit -> swizzled smem -> TMA store
+        if (!aborted && n > 0) aborted = !wait_warp(bar_o(n - 1), ((n - 1) >> 1) & 1, abort, tmo);
+        // a tile that sees no key stages its zeros over the Q tile: wait until
+        // the copy of Q has landed, or it could overwrite them
+        if (!SPLIT && !aborted && n == 0) aborted = !wait_warp(bar_q, 0, abort, tmo);
+        const float l_all = lsum.x + lsum.y;
+        const float lhat_all = lhat.x + lhat.y;
+        if constexpr (SPLIT) {
+            if (!aborted) {
+                const bool mine = row < p.Nq && !*abort;
+                const bool any = l_all > 0.f;
+                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (mine ? row : 0);
+                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
+                if (mine) {
+                    p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
+                    p.lse_part[plane + i] = any ? m_ref * p.scale + logf(lhat_all) : -INFINITY;
+                }
+                ptx::tc_fence_after_sync();
+                const float inv = any ? 1.f / lhat_all : 0.f;
+                float4* dst = reinterpret_cast<float4*>(p.o_part + i * D);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; u += 4) {
+                        ptx::reg_fence(ov[u]);
+                        ptx::reg_fence(ov[u + 1]);
+                        ptx::reg_fence(ov[u + 2]);
+                        ptx::reg_fence(ov[u + 3]);
+                        if (mine)
+                            dst[c * 8 + u / 4] = make_float4(
+                                __uint_as_float(ov[u]) * inv, __uint_as_float(ov[u + 1]) * inv,
+                                __uint_as_float(ov[u + 2]) * inv, __uint_as_float(ov[u + 3]) * inv);
+                    }
+                }
+            }
+        } else if (!aborted) {
+            ptx::tc_fence_after_sync();
+            const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
+            const float2 iv = make_float2(inv, inv);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                if (n > 0) {
+                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ptx::reg_fence(ov[u]);
+                } else {  // no key visible to this tile: O = 0 (U was never written)
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ov[u] = 0u;
+                }
+                // the Q tile is free now (every S product is done) and becomes
+                // the staging buffer, 128-byte swizzled as the TMA store expects
+                const uint32_t sub = sQ + (c >> 1) * C::kQSubBytes + t * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk = (c & 1) * 4 + q4;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int u = q4 * 8 + 2 * e;
+                        const float2 o2 = __fmul2_rn(
+                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), iv);
+                        w[e] = pack2<BF16>(o2.x, o2.y);
+                    }
+                    const uint32_t dst = sub + ((chunk ^ (t & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]),
+                                 "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            }
+            ptx::fence_proxy_async_smem();
+        }
+        ptx::named_barrier_sync(1, kTileM);
+        if (!SPLIT && t == 0 && !*abort) {
+#pragma unroll
+            for (int c = 0; c < C::kSub; ++c)
+                ptx::tma_store_4d(&tm_o, sQ + c * C::kQSubBytes, 64 * c, first_row, h_idx, b_idx);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read0();
+        }
+        if (!SPLIT && !aborted && !*abort && row < p.Nq) {
+            const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
+            p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
+        }
+    }
+
+    // ---- teardown: every tcgen05 op of this CTA has completed
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    if (warp == kWideMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace fa

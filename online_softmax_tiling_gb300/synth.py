@@ -149,6 +149,8 @@ WORKLOADS = {
                  note="walkthrough shape: L=128, D=64, BlockM=BlockN=64"),
         Workload("C2_b1h1n4096d64_fp16", 1, 1, 4096, 64, FP16, 1 / 8, False, 2000,
                  note="the HBM-traffic example shape, one head"),
+        Workload("C2x16_b1h16n4096d64_fp16", 1, 16, 4096, 64, FP16, 1 / 8, False, 2100,
+                 note="the traffic example shape, 16 heads: S and P (512 MiB each) exceed L2"),
         Workload("C3_b4h16n4096d64_fp16_causal", 4, 16, 4096, 64, FP16, 1 / 8, True, 3000),
         Workload("C4_b2h32n8192d128_bf16", 2, 32, 8192, 128, BF16, 1 / math.sqrt(128), False,
                  4000, qk_mult=2.0, note="Q, K drawn with std 2 to widen the score range"),
@@ -160,6 +162,13 @@ WORKLOADS = {
                  6000, note="N=4096, d=128 non-causal throughput point"),
         Workload("T_b2h32n4096d128_fp16", 2, 32, 4096, 128, FP16, 1 / math.sqrt(128), False,
                  7000),
+        Workload("D256_b2h16n4096d256_bf16", 2, 16, 4096, 256, BF16, 1 / 16, False, 8000,
+                 note="wide head: same FLOPs per launch as T, d=256"),
+        Workload("D256c_b2h16n4096d256_bf16_causal", 2, 16, 4096, 256, BF16, 1 / 16, True, 8100),
+        Workload("D192_b2h16n4096d192_bf16", 2, 16, 4096, 192, BF16, 1 / math.sqrt(192), False,
+                 8200),
+        Workload("D96_b2h32n4096d96_bf16", 2, 32, 4096, 96, BF16, 1 / math.sqrt(96), False, 8300,
+                 note="d=96 served by the 128-wide kernel with zero-filled columns"),
     ]
 }
 

@@ -1,4 +1,4 @@
-"""The C-ABI library loads, exports what include/fa.h declares, and rejects bad
+"""The C-ABI library loads, exports what include/*.h declare, and rejects bad
 arguments on the host (no GPU needed: these paths return before any CUDA call)."""
 import os
 import re
@@ -11,9 +11,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "fa.h"), encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for h in sorted(os.listdir(inc)):
+        if h.endswith(".h"):
+            text = open(os.path.join(inc, h), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -63,7 +68,9 @@ def _call(**kw):
     (dict(scale=-0.1), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
-    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=100), fa.FA_ERR_UNSUPPORTED),   # not a multiple of 8 (16-byte rows)
+    (dict(d=264), fa.FA_ERR_UNSUPPORTED),   # wider than the widest kernel
+    (dict(d=4), fa.FA_ERR_UNSUPPORTED),
     (dict(d=0), fa.FA_ERR_UNSUPPORTED),
     (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
@@ -97,6 +104,16 @@ def test_splitkv_workspace_size_and_validation(lib):
     assert fa.fa_fwd_splitkv(*base, 4, ws, need - 1, None) == fa.FA_ERR_INVALID_ARG
     assert 1 <= fa.fa_splitkv_num_splits(1, 1, 4096, 64, 0) <= fa.FA_MAX_SPLITS
     assert fa.fa_splitkv_num_splits(64, 64, 4096, 128, 0) == 1
+    assert fa.fa_splitkv_num_splits(1, 1, 4096, 100, 0) == 1      # unsupported d: no split
+
+
+@pytest.mark.parametrize("d,width", [(8, 64), (64, 64), (72, 128), (96, 128), (128, 128),
+                                     (136, 192), (192, 192), (200, 256), (256, 256)])
+def test_splitkv_workspace_uses_the_kernel_width(lib, d, width):
+    """Partial O rows are as wide as the kernel that serves d (64, 128, 192 or 256)."""
+    S, BH, N = 3, 2, 500
+    o_bytes = (4 * S * BH * N * width + 255) // 256 * 256
+    assert fa.fa_splitkv_workspace_size(1, 2, N, d, S) == o_bytes + 4 * 2 * S * BH * N
 
 
 def test_fa_fwd_ex_validation(lib):
@@ -119,7 +136,31 @@ def test_fa_fwd_ex_validation(lib):
     assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG
     a.Nk, a.lse_stride[1] = 300, 0
     assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG
-    a.lse_stride[1], a.d = 100, 80
+    a.lse_stride[1], a.d = 100, 84
     assert fa.fa_fwd_ex(a) == fa.FA_ERR_UNSUPPORTED
     a.d, a.num_splits, a.workspace = 64, 4, None
     assert fa.fa_fwd_ex(a) == fa.FA_ERR_INVALID_ARG          # split without a workspace
+
+
+def test_ceiling_probes_validate_arguments(lib):
+    import ctypes
+    assert lib.fa_ceiling_ex2_rate(None, None) == fa.FA_CEIL_ERR_ARG
+    out = ctypes.c_double()
+    assert lib.fa_ceiling_l2_read(None, 1 << 20, ctypes.byref(out), None) == fa.FA_CEIL_ERR_ARG
+    assert lib.fa_ceiling_l2_read(ctypes.c_void_p(A), 1000, ctypes.byref(out), None) == fa.FA_CEIL_ERR_ARG
+    assert lib.fa_ceiling_l2_read(ctypes.c_void_p(A + 8), 1 << 20, ctypes.byref(out), None) == \
+        fa.FA_CEIL_ERR_ARG
+
+
+def test_naive_validation(lib):
+    base = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 2, 1000, 64, 0.125, 0, fa.FA_FP16)
+    need = fa.fa_naive_workspace_size(1, 2, 1000)
+    assert need == 2 * ((2 * 1000 * 1000 * 2 + 255) // 256 * 256)   # S and P, 16-bit each
+    ws = 0x100000
+    assert fa.fa_naive_fwd(*base, ws, need - 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_naive_fwd(*base, None, need, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_naive_fwd(*base, ws + 16, need, None) == fa.FA_ERR_MISALIGNED
+    b = list(base); b[7] = 1001                                     # N not a multiple of 8
+    assert fa.fa_naive_fwd(*b, ws, need, None) == fa.FA_ERR_UNSUPPORTED
+    b = list(base); b[8] = 96
+    assert fa.fa_naive_fwd(*b, ws, need, None) == fa.FA_ERR_UNSUPPORTED

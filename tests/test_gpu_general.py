@@ -22,25 +22,6 @@ def _cuda():
     yield
 
 
-def _check(q, k, v, dtype, mask, o_dev, lse_dev, label):
-    """Compare device outputs (torch, any strides) with the oracle on every row."""
-    import torch
-    B, H, Nq, d = q.shape
-    o = parity.from_device(o_dev.contiguous()).reshape(-1, d)
-    lse = lse_dev.contiguous().cpu().numpy().reshape(-1)
-    rows = np.arange(B * H * Nq, dtype=np.int64)
-    scale = 1.0 / math.sqrt(d)
-    o_ref, lse_ref, spread = oracle.attention_rows16(q, k, v, dtype, scale, mask, rows,
-                                                     with_spread=True)
-    empty = np.isneginf(lse_ref)          # rows that see no key: O = 0, LSE = -inf
-    if empty.any():
-        assert np.all(synth.bits_to_float(o[empty], dtype) == 0.0), label
-        assert np.all(np.isneginf(lse[empty])), label
-    keep = ~empty
-    st = parity.compare(o[keep], lse[keep], o_ref[keep], lse_ref[keep], spread[keep], dtype)
-    parity.assert_within(st, label)
-
-
 CASES = [  # (B, H, Nq, Nk, d, dtype, mask)
     (1, 2, 300, 700, 128, synth.BF16, 0),
     (1, 2, 300, 700, 128, synth.BF16, 1),
@@ -64,7 +45,7 @@ def test_unequal_lengths_and_masks(B, H, Nq, Nk, d, dtype, mask, splits):
     qd, kd, vd = (parity.to_device(x, dtype) for x in (q, k, v))
     o, lse = fa.attention_forward_ex(qd, kd, vd, mask=mask, num_splits=splits)
     assert fa.fa_check_device_status(None) == fa.FA_OK
-    _check(q, k, v, dtype, mask, o, lse, f"Nq{Nq} Nk{Nk} mask{mask} splits{splits}")
+    parity.check_rows(q, k, v, dtype, mask, o, lse, f"Nq{Nq} Nk{Nk} mask{mask} splits{splits}")
 
 
 def test_strided_bshd_views_in_and_out():
@@ -84,7 +65,7 @@ def test_strided_bshd_views_in_and_out():
                                          lse=lse_store[:, :, :N])
         assert fa.fa_check_device_status(None) == fa.FA_OK
         assert (lse_store[:, :, N:] == -1.0).all()           # padding untouched
-        _check(q, k, v, dtype, mask, o, lse, f"bshd mask{mask}")
+        parity.check_rows(q, k, v, dtype, mask, o, lse, f"bshd mask{mask}")
 
 
 def test_ex_matches_fa_fwd_bitwise_on_contiguous():
