@@ -140,6 +140,11 @@ int fa_fwd_ex(const fa_fwd_args* args);
  * then about one wave of CTAs, with at least four key tiles per range. */
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal);
 
+/* The split count fa_fwd_ex chooses for num_splits = 0 with these arguments:
+ * as fa_splitkv_num_splits, with the keys per range counted from Nk (so one
+ * query row against a long key sequence, as in decoding, is split). */
+int fa_splitkv_num_splits_ex(const fa_fwd_args* args);
+
 /* Workspace bytes fa_fwd_splitkv needs for num_splits >= 2 (0 otherwise, or
  * for an unsupported d).  Partial O rows are as wide as the kernel serving d. */
 size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);

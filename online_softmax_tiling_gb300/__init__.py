@@ -25,7 +25,7 @@ LIBRARY = os.path.join(_HERE, "libfa_gb300.so")
 EXPORTS = ("fa_fwd", "fa_check_device_status", "fa_status_string", "fa_version", "fa_fwd_debug",
            "fa_splitkv_num_splits", "fa_splitkv_workspace_size", "fa_fwd_splitkv",
            "fa_fwd_splitkv_noalloc", "fa_fwd_ex", "fa_ceiling_ex2_rate", "fa_ceiling_l2_read",
-           "fa_naive_fwd", "fa_naive_workspace_size")
+           "fa_naive_fwd", "fa_naive_workspace_size", "fa_splitkv_num_splits_ex")
 FA_CEIL_OK, FA_CEIL_ERR_ARG, FA_CEIL_ERR_CUDA = 0, 1, 4
 FA_MASK_NONE, FA_MASK_CAUSAL_TOP_LEFT, FA_MASK_CAUSAL_BOTTOM_RIGHT = 0, 1, 2
 
@@ -89,6 +89,8 @@ def library() -> ctypes.CDLL:
             lib.fa_fwd_splitkv_noalloc.restype = i
             lib.fa_fwd_ex.argtypes = [ctypes.POINTER(fa_fwd_args)]
             lib.fa_fwd_ex.restype = i
+            lib.fa_splitkv_num_splits_ex.argtypes = [ctypes.POINTER(fa_fwd_args)]
+            lib.fa_splitkv_num_splits_ex.restype = i
             lib.fa_ceiling_ex2_rate.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
             lib.fa_ceiling_ex2_rate.restype = i
             lib.fa_ceiling_l2_read.argtypes = [vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_double), vp]
@@ -180,6 +182,11 @@ def fa_ceiling_l2_read(buf, nbytes: int, stream=None) -> float:
         raise FaError(FA_ERR_CUDA if st == FA_CEIL_ERR_CUDA else FA_ERR_INVALID_ARG,
                       "fa_ceiling_l2_read")
     return out.value
+
+
+def fa_splitkv_num_splits_ex(args: "fa_fwd_args") -> int:
+    """Split count fa_fwd_ex uses for num_splits = 0 with these arguments."""
+    return library().fa_splitkv_num_splits_ex(ctypes.byref(args))
 
 
 def fa_check_device_status(stream=None) -> int:
@@ -287,7 +294,7 @@ def attention_forward_ex(q, k, v, scale: float | None = None, mask: int = FA_MAS
     a.lse_stride[:] = [lse.stride(0), lse.stride(1)]
     a.scale, a.mask, a.dtype = float(scale), int(mask), _dtype_code(q)
     if num_splits == 0:
-        num_splits = fa_splitkv_num_splits(B, H, Nq, d, int(mask != FA_MASK_NONE))
+        num_splits = fa_splitkv_num_splits_ex(a)
     a.num_splits = num_splits
     ws = None
     if num_splits > 1:

@@ -152,6 +152,25 @@ size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
     return split_o_bytes(S, BH, N, d) + static_cast<size_t>(2 * S * BH * N) * 4;
 }
 
+// Split count for BH heads of Nq query rows and Nk keys on a kernel of
+// width kd.  Splitting pays for its fp32 partials and merge only when most
+// SMs would otherwise idle: split when the query blocks fill less than half
+// of them, into about one wave of CTAs, keeping at least 512 keys per range.
+int choose_splits(int64_t BH, int Nq, int Nk, int kd) {
+    if (kd == 0) return 1;
+    int device = 0, sms = 148;
+    if (cudaGetDevice(&device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        sms = 148;
+    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t ctas = BH * ((Nq + block_m - 1) / block_m);
+    if (2 * ctas > sms) return 1;
+    int64_t s = (static_cast<int64_t>(sms) + ctas - 1) / ctas;
+    s = std::min<int64_t>(s, std::max<int64_t>(1, static_cast<int64_t>(Nk) / 512));
+    s = std::min<int64_t>(s, FA_MAX_SPLITS);
+    return static_cast<int>(std::max<int64_t>(1, s));
+}
+
 // Contiguous [B, H, N, d] strides.
 fa_fwd_args contiguous_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                             int H, int N, int d, float scale, int causal, int dtype, void* stream) {
@@ -203,8 +222,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         misaligned(a.lse, 4))
         return FA_ERR_MISALIGNED;
     int num_splits = a.num_splits;
-    if (num_splits == 0)
-        num_splits = fa_splitkv_num_splits(B, H, Nq, d, a.mask != FA_MASK_NONE);
+    if (num_splits == 0) num_splits = choose_splits(static_cast<int64_t>(B) * H, Nq, Nk, kernel_dim(d));
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
     const bool split = num_splits > 1;
     if (split) {
@@ -302,22 +320,13 @@ int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* ls
 
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
     (void)causal;
-    const int kd = kernel_dim(d);
-    if (B < 1 || H < 1 || N < 1 || kd == 0) return 1;
-    int device = 0, sms = 148;
-    if (cudaGetDevice(&device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-        sms = 148;
-    // Splitting pays for its fp32 partials and merge only when most SMs would
-    // otherwise idle: split when the blocks fill less than half of them, into
-    // about one wave, keeping at least 512 keys per range.
-    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
-    const int64_t ctas = static_cast<int64_t>(B) * H * ((N + block_m - 1) / block_m);
-    if (2 * ctas > sms) return 1;
-    int64_t s = (static_cast<int64_t>(sms) + ctas - 1) / ctas;
-    s = std::min<int64_t>(s, std::max<int64_t>(1, static_cast<int64_t>(N) / 512));
-    s = std::min<int64_t>(s, FA_MAX_SPLITS);
-    return static_cast<int>(std::max<int64_t>(1, s));
+    if (B < 1 || H < 1 || N < 1) return 1;
+    return choose_splits(static_cast<int64_t>(B) * H, N, N, kernel_dim(d));
+}
+
+int fa_splitkv_num_splits_ex(const fa_fwd_args* a) {
+    if (!a || a->B < 1 || a->H < 1 || a->Nq < 1 || a->Nk < 1) return 1;
+    return choose_splits(static_cast<int64_t>(a->B) * a->H, a->Nq, a->Nk, kernel_dim(a->d));
 }
 
 size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {

@@ -164,3 +164,14 @@ def test_naive_validation(lib):
     assert fa.fa_naive_fwd(*b, ws, need, None) == fa.FA_ERR_UNSUPPORTED
     b = list(base); b[8] = 96
     assert fa.fa_naive_fwd(*b, ws, need, None) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_split_choice_counts_keys_from_nk(lib):
+    a = fa.fa_fwd_args()
+    a.B, a.H, a.Nq, a.Nk, a.d = 1, 8, 1, 262144, 128
+    assert fa.fa_splitkv_num_splits_ex(a) > 1                  # decoding: one row, many keys
+    a.Nk = 256
+    assert fa.fa_splitkv_num_splits_ex(a) == 1                 # too few keys to split
+    a.B, a.H, a.Nq, a.Nk = 2, 32, 4096, 4096
+    assert fa.fa_splitkv_num_splits_ex(a) == 1                 # the grid already fills the GPU
+    assert lib.fa_splitkv_num_splits_ex(None) == 1
