@@ -186,11 +186,11 @@ def kernel_width(d: int) -> int:
 def ceiling_counts(w: synth.Workload) -> dict:
     """Per launch of the fused kernel: 2^x evaluations (one per visible query,
     key pair) and bytes read from L2 into the SMs (each CTA's Q tile and the K
-    and V tiles it visits; tiles of 128 keys for d <= 128 with two 128-row
-    query tiles per CTA, 64 keys and one query tile per CTA above)."""
+    and V tiles it visits; tiles of 128 keys, with two 128-row query tiles per
+    CTA for d <= 128 and one above)."""
     B, H, N, d = w.shape
     wide = kernel_width(d) > 128
-    bm, bn = (128, 64) if wide else (256, 128)
+    bm, bn = (128, 128) if wide else (256, 128)
     nkv = -(-N // bn)
     tiles = 0
     for qb in range(-(-N // bm)):

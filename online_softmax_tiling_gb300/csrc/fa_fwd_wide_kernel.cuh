@@ -12,13 +12,18 @@
 //   * one CTA per 128-row query tile; 6 warps: warps 0-3 softmax + epilogue
 //     (thread t owns row t = TMEM lane t), warp 4 the TMA loader, warp 5 the
 //     tensor-core issuer;
-//   * key tiles of 64 keys (K and V tiles of 64 x d, 2-3 stages each);
-//   * TMEM: two score buffers S0 at column 0 and S1 at 64 (64 fp32 columns;
-//     the weights P overwrite the first 32), U at column 128 (d columns);
+//   * key tiles of 128 keys, so that S = Q K^T runs as M128 N128 products
+//     (an N64 product takes 48 cycles for 32 cycles of work); K and V tiles
+//     of 128 x d fit once each in shared memory next to Q for d = 256 (K
+//     twice for d = 192), so each tile loads while the product before its
+//     first use runs;
+//   * TMEM: two score buffers S0 at column 0 and S1 at 128 (128 fp32
+//     columns; the weights P overwrite the first 64), U at column 256 (d
+//     columns);
 //   * tensor-core order: S(0), S(1), then per key tile j: PV(j), S(j+2).
 //     The softmax of tile j+1 runs while the tensor core computes PV(j) and
-//     S(j+2) - with d = 256 each is 512 cycles, so the softmax of 64 keys
-//     (about half that) stays off the critical path.
+//     S(j+2) - with d = 256 each is 1024 cycles, so the softmax of 128 keys
+//     (about 1200 cycles) stays off the critical path.
 //   * S(j+1) is issued before PV(j), so U may still be absorbing P(j-1) V
 //     when the softmax of tile j wants to rescale it: that (rare) rescale
 //     first waits for PV(j-1).  Each score buffer has its own "weights
@@ -34,22 +39,22 @@
 
 namespace fa {
 
-constexpr int kWideBlockN = 64;      // keys per tile
+constexpr int kWideBlockN = 128;     // keys per tile
 constexpr int kWideThreads = 192;    // 4 softmax warps + loader warp + MMA warp
 constexpr int kWideLoaderWarp = 4;
 constexpr int kWideMmaWarp = 5;
-constexpr uint32_t kWideTmemU = 128;  // S0 at 0, S1 at 64, U at 128
+constexpr uint32_t kWideTmemU = 256;  // S0 at 0, S1 at 128, U at 256
 
 template <int D>
 struct WideCfg {
     static_assert(D == 192 || D == 256, "wide head dim");
     static constexpr int kSub = D / 64;                      // 64-column swizzle sub-tiles
     static constexpr int kQSubBytes = kTileM * 128;          // 128 rows x 128 bytes
-    static constexpr int kKVSubBytes = kWideBlockN * 128;    // 64 rows x 128 bytes
+    static constexpr int kKVSubBytes = kWideBlockN * 128;    // 128 rows x 128 bytes
     static constexpr int kQBytes = kSub * kQSubBytes;
     static constexpr int kKVBytes = kSub * kKVSubBytes;
-    static constexpr int kKStages = D == 256 ? 2 : 3;
-    static constexpr int kVStages = D == 256 ? 2 : 3;
+    static constexpr int kKStages = D == 256 ? 1 : 2;
+    static constexpr int kVStages = 1;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             __syncwarp();
         };
-        // U (+)= P_b V_s: 64 keys = 4 steps of K16; P advances 8 TMEM columns
+        // U (+)= P_b V_s: 128 keys = 8 steps of K16; P advances 8 TMEM columns
         // (16 packed 16-bit weights), V 16 rows = 2048 bytes per step
         auto issue_pv = [&](int b, int s, bool acc) {
             if (ptx::elect_one()) {
@@ -398,7 +403,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
             lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
             lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
-            ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+                ptx::tmem_st_32x32b_x32(s_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
             // U may still be absorbing P(j-1) V (issued after S(j)): a rescale
             // waits for that product first (warp-uniform)
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
