@@ -473,9 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // see (>= Nk, or past the causal limit) masked to -inf
         auto load_scores = [&](uint32_t(&sv)[kBlockN], int j) {
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c)
-                ptx::tmem_ld_32x32b_x32(s_addr + c * 32,
-                                        *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+            for (int c = 0; c < kBlockN / 64; ++c)
+                ptx::tmem_ld_32x32b_x64(s_addr + c * 64,
+                                        *reinterpret_cast<uint32_t(*)[64]>(&sv[c * 64]));
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kBlockN; ++c) ptx::reg_fence(sv[c]);
