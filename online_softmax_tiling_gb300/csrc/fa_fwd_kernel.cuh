@@ -24,17 +24,23 @@
 //   * tensor-core order per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).
 //     While the softmax warps of tile A turn S_A(j+1) into weights, the tensor
 //     core works on tile B (and vice versa), so the two softmax groups and the
-//     tensor core overlap.  Because S_X(j+1) is issued after PV_X(j), its
-//     completion also means U_X holds P_X(j) V_j: the softmax warps may
-//     rescale U_X right away, without another wait.
+//     tensor core overlap.  Each PV_X(j) runs in two halves of 64 keys: the
+//     softmax warps hand over the weights of keys 0-63 before computing those
+//     of keys 64-127, so the first half of the product runs meanwhile and
+//     only the second half and S_X(j+1) remain between the end of one
+//     softmax and the start of the next.  Because S_X(j+1) is issued after
+//     PV_X(j), its completion also means U_X holds P_X(j) V_j: the softmax
+//     warps may rescale U_X right away, without another wait.
 //   * weights are computed against the running reference maximum m of the
 //     previous tiles, without taking the new tile's maximum first; their fp32
 //     sum bounds every weight (all are >= 0), so while it stays below a bound
 //     that keeps each weight inside the 16-bit type, l, U and the weights keep
 //     the old reference, which is exact because l, U and LSE all refer to the
-//     same m.  Only the first tile of a row, or a tile whose weights would
+//     same m.  Only the first tile of a row, or a tile whose first half would
 //     pass the bound, takes the tile maximum, moves m, rescales U in TMEM and
-//     recomputes the weights from the scores still in TMEM.
+//     recomputes the weights from the scores still in TMEM.  A second half
+//     that would pass it moves m to that half's maximum once U has absorbed
+//     the first half (which carries the old reference like the rest of U).
 //   * O is normalised by the sum of the 16-bit weights actually fed to P.V,
 //     so it is an exact convex combination of those weights; LSE uses the sum
 //     of the fp32 weights.
@@ -109,7 +115,9 @@ struct alignas(8) Ctl {
     uint64_t v_full[NV];
     uint64_t v_empty[NV];
     uint64_t s_full[2];   // per query tile: S_X(j) is in TMEM
-    uint64_t p_full[2];   // per query tile: P_X(j) is in TMEM (and U_X rescaled)
+    uint64_t p_half[2];   // per query tile: the weights of keys 0-63 of tile j are in TMEM
+    uint64_t p_full[2];   // per query tile: all of P_X(j) is in TMEM (and U_X rescaled)
+    uint64_t o_half[2];   // per query tile: U_X has absorbed keys 0-63 of P_X(j) V_j
     uint64_t o_ready[2];  // per query tile: U_X has absorbed P_X(j) V_j
     uint64_t drain;
     uint32_t tmem_base;
@@ -278,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar_vf = [&](int s) { return ptx::smem_addr(&ctl->v_full[s]); };
     auto bar_ve = [&](int s) { return ptx::smem_addr(&ctl->v_empty[s]); };
     auto bar_sf = [&](int x) { return ptx::smem_addr(&ctl->s_full[x]); };
+    auto bar_ph = [&](int x) { return ptx::smem_addr(&ctl->p_half[x]); };
     auto bar_pf = [&](int x) { return ptx::smem_addr(&ctl->p_full[x]); };
+    auto bar_oh = [&](int x) { return ptx::smem_addr(&ctl->o_half[x]); };
     auto bar_o = [&](int x) { return ptx::smem_addr(&ctl->o_ready[x]); };
     const uint32_t bar_drain = ptx::smem_addr(&ctl->drain);
     auto sQ = [&](int x) { return sbase + C::kOffQ + x * C::kTileBytes; };
@@ -297,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int x = 0; x < 2; ++x) {
             ptx::mbar_init(bar_sf(x), 1);
+            ptx::mbar_init(bar_ph(x), kTileM);
             ptx::mbar_init(bar_pf(x), kTileM);
+            ptx::mbar_init(bar_oh(x), 1);
             ptx::mbar_init(bar_o(x), 1);
         }
         ptx::mbar_init(bar_drain, 1);
@@ -390,10 +402,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 ptx::mma_ss_k64(tmem + x * 128, qd, kd, idesc_s, 0u);
         };
-        // U_x (+)= P_x V_s, P_x read from TMEM: 128 keys = 8 K-steps of 16
-        auto issue_pv = [&](int x, int s, bool acc) {
-            ptx::mma_ts_k128(tmem + kTmemU + x * 128, tmem + x * 128, v_desc0 + s * kTileStep,
-                             idesc_pv, acc ? 1u : 0u);
+        // U_x (+)= P_x V_s, P_x read from TMEM, in two halves of 64 keys (4
+        // K-steps of 16 each): the first half runs while the softmax warps
+        // still compute the weights of the second
+        auto issue_pv = [&](int x, int s, int half, bool acc) {
+            ptx::mma_ts_k64(tmem + kTmemU + x * 128, tmem + x * 128 + half * 32,
+                            v_desc0 + s * kTileStep + half * 512, idesc_pv, acc ? 1u : 0u);
+        };
+        // both halves of P_x(j) V_j, each issued once the softmax warps have
+        // written its weights; o_half / o_ready signal that U_x absorbed them
+        auto pv_tile = [&](int x, int s, int j) {
+            if (!wait_warp(bar_ph(x), j & 1, abort, tmo)) return false;
+            ptx::tc_fence_after_sync();
+            issue_pv(x, s, 0, j > 0);
+            ptx::tc_commit_elect(bar_oh(x));
+            if (!wait_warp(bar_pf(x), j & 1, abort, tmo)) return false;
+            ptx::tc_fence_after_sync();
+            issue_pv(x, s, 1, true);
+            ptx::tc_commit_elect(bar_o(x));
+            return true;
         };
         bool ok = nB > 0 && wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
         if (ok) {
@@ -413,10 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool k_ready = false;
             if (!(ok = wait_warp(bar_vf(sv), (j / NV) & 1, abort, tmo))) break;
             if (j < nA) {
-                if (!(ok = wait_warp(bar_pf(0), j & 1, abort, tmo))) break;
-                ptx::tc_fence_after_sync();
-                issue_pv(0, sv, j > 0);
-                ptx::tc_commit_elect(bar_o(0));
+                if (!(ok = pv_tile(0, sv, j))) break;
                 if (j + 1 < nA) {
                     if (!(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
                     k_ready = true;
@@ -426,10 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
             }
-            if (!(ok = wait_warp(bar_pf(1), j & 1, abort, tmo))) break;
-            ptx::tc_fence_after_sync();
-            issue_pv(1, sv, j > 0);
-            ptx::tc_commit_elect(bar_o(1));
+            if (!(ok = pv_tile(1, sv, j))) break;
             if (j + 1 < nB) {
                 if (!k_ready && !(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
                 ptx::tc_fence_after_sync();
@@ -525,24 +546,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after_sync();
+            // keys 0-63 of tile j-1 are in U_x (S_x(j) was issued after them);
+            // taking that phase here keeps a later wait on phase j unambiguous
+            if (j > 0 && !wait_warp(bar_oh(x), (j - 1) & 1, abort, tmo)) {
+                aborted = true;
+                break;
+            }
             // common case: weights against the current reference, checked by
-            // their sum before they are written; the first tile (no reference
-            // yet) or a sum above the bound takes the tile maximum and
-            // recomputes from the scores still in TMEM (warp-uniform)
+            // their sum before they are written, one 64-key half at a time: the
+            // first half goes to the tensor core while the second is computed.
+            // The first tile (no reference yet) or a first half above the bound
+            // takes the tile maximum and recomputes all weights from the scores
+            // still in TMEM; a second half above the bound moves the reference
+            // for that half only (all branches warp-uniform).
             uint32_t pk[kBlockN / 2];
-            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // keys 64-127 (or all)
             float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float r1 = 0.f, h1 = 0.f;  // sums of keys 0-63 when they were sent on the old reference
             // (tcgen05.ld is warp-collective: every branch around it is uniform)
             bool redo = (m_ref == -INFINITY);
+            bool half_sent = false;
+            float alpha = 1.f;
+            float m_new = m_ref;
             if (!__any_sync(0xffffffffu, redo)) {
                 uint32_t sv[kBlockN];
                 load_scores(sv, j);
-                weights(sv, kBlockN / 2, -m_ref * c2, pk, rs, rh);
-                redo = rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
+                float2 s1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float2 t1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                weights(sv, kBlockN / 4, -m_ref * c2, pk, s1, t1);
+                r1 = s1[0].x + s1[0].y + s1[1].x + s1[1].y;
+                redo = r1 > weight_sum_limit<BF16>();
+                if (!__any_sync(0xffffffffu, redo)) {
+                    ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before_sync();
+                    ptx::mbar_arrive(bar_ph(x));
+                    half_sent = true;
+                    const float2 h = __fadd2_rn(t1[0], t1[1]);
+                    h1 = h.x + h.y;
+                    weights(sv + kBlockN / 2, kBlockN / 4, -m_ref * c2, pk + kBlockN / 4, rs, rh);
+                    const bool redo2 =
+                        rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
+                    if (__any_sync(0xffffffffu, redo2)) {
+                        float mt = -INFINITY;
+#pragma unroll 1
+                        for (int c = 2; c < kBlockN / 32; ++c) {
+                            uint32_t sc[32];
+                            load_chunk(sc, c, j);
+#pragma unroll
+                            for (int u = 0; u < 32; u += 2)
+                                mt = ptx::fmax3(mt, __uint_as_float(sc[u]), __uint_as_float(sc[u + 1]));
+                        }
+                        if (redo2) {
+                            m_new = fmaxf(mt, m_ref);
+                            alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                        }
+                        rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int c = 2; c < kBlockN / 32; ++c) {
+                            uint32_t sc[32];
+                            load_chunk(sc, c, j);
+                            weights(sc, 16, -m_new * c2, &pk[16 * c], rs, rh);
+                        }
+                    }
+                } else {
+                    r1 = 0.f;
+                }
             }
-            float alpha = 1.f;
-            float m_new = m_ref;
-            if (__any_sync(0xffffffffu, redo)) {
+            if (!half_sent) {
                 float mt = -INFINITY;
 #pragma unroll 1
                 for (int c = 0; c < kBlockN / 32; ++c) {
@@ -561,30 +632,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
                     mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
                 }
-                // lanes whose weights were in range keep their reference
-                if (redo) {
-                    m_new = fmaxf(mt, m_ref);
-                    if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
-                }
+                // every lane takes the tile maximum: a lane whose first half
+                // was in range may still overflow in its second half, which
+                // was never checked (alpha is exactly 1 where m does not move)
+                m_new = fmaxf(mt, m_ref);
+                if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
                 // a row with no valid key so far keeps all weights at zero
                 const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
-                rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < kBlockN / 32; ++c) {
                     uint32_t sv[32];
                     load_chunk(sv, c, j);
                     weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
                 }
+                ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
             }
-            const float2 av = make_float2(alpha, alpha);
+            // l = alpha (l + keys sent on the old reference) + the rest
             const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
-            lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
-            lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
-            ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+            lsum.x = fmaf(lsum.x + r1, alpha, r.x + r.y);
+            lhat.x = fmaf(lhat.x + h1, alpha, hh.x + hh.y);
             ptx::tmem_st_32x32b_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-            // U_x already holds P(j-1) V: S_x(j) was issued after that product.
-            // Rescale it by alpha when the reference maximum moved (warp-uniform).
+            // U_x holds P(j-1) V, since S_x(j) was issued after that product.
+            // Rescale it by alpha when the reference maximum moved (warp-uniform);
+            // if keys 0-63 of this tile were already sent, U_x must absorb them
+            // first: they carry the old reference too.
             if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (half_sent) {
+                    if (!wait_warp(bar_oh(x), j & 1, abort, tmo)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                }
+                const float2 av = make_float2(alpha, alpha);
 #pragma unroll 1
                 for (int c = 0; c < D / 16; ++c) {
                     uint32_t ov[16];
@@ -604,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before_sync();
+            if (!half_sent) ptx::mbar_arrive(bar_ph(x));
             ptx::mbar_arrive(bar_pf(x));
             m_ref = m_new;
         }

@@ -309,6 +309,26 @@ __device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// TS form, K = 64 keys (one half of a 128-key tile): 4 steps.  The second
+// half of a tile starts 32 TMEM columns and 64 V rows further on.
+__device__ __forceinline__ void mma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
+        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Maximum of three values (sm_100+ three-input form).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;

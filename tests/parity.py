@@ -138,3 +138,63 @@ def check_rows(q, k, v, dtype, mask, o_dev, lse_dev, label):
     st = compare(o[keep], lse[keep], o_ref[keep], lse_ref[keep], spread[keep], dtype)
     assert_within(st, label)
     return st
+
+
+def keys_growing_by_half(dtype, d, seed=611, B=1, H=2, N=1000, growth=None):
+    """Q, K, V whose key magnitudes grow every 64 keys, i.e. from the first to
+    the second half of every 128-key tile of the kernel: the weights of a
+    later half overflow the bound against the reference of the earlier keys
+    (the growth is smaller for fp16, whose bound is smaller)."""
+    if growth is None:
+        growth = 8.0 if dtype == synth.FP16 else 16.0
+    q = synth.tensor_bits(seed, (B, H, N, d), dtype)
+    kf = synth.bits_to_float(synth.tensor_bits(seed + 1, (B, H, N, d), dtype), dtype)
+    kf = kf.astype(np.float64) * (1.0 + growth * (np.arange(N) // 64) / 15.0)[None, None, :, None]
+    k = synth.round_to_bits(kf, dtype)
+    v = synth.tensor_bits(seed + 2, (B, H, N, d), dtype)
+    return q, k, v
+
+
+def softmax_paths(q_bits, k_bits, dtype, scale, causal):
+    """Which route the kernel's softmax takes per (row, key tile), counted as
+    (full tile, second half only, common).  This restates the kernel's
+    control decisions (not the method's arithmetic) in float64, to check that
+    test inputs reach every route.  Decisions are made per warp of 32
+    consecutive rows: if any row of the warp has no reference yet (its first
+    tile) or a first half of 64 keys whose weights against the running
+    reference sum above the bound (2^15 fp16, 2^32 bf16), every row of the
+    warp re-takes the maximum of the whole tile; otherwise, if any row's
+    second half passes the bound, those rows re-take the maximum of that
+    half."""
+    lim = 4294967296.0 if dtype == synth.BF16 else 32768.0
+    c2 = scale * math.log2(math.e)
+    qf = synth.bits_to_float(q_bits, dtype).astype(np.float64)
+    kf = synth.bits_to_float(k_bits, dtype).astype(np.float64)
+    B, H, N, _ = qf.shape
+    counts = np.zeros(3, dtype=np.int64)
+    rows = np.arange(N)
+    warp = rows // 32
+
+    def per_warp(flag):
+        return np.bincount(warp, weights=flag.astype(np.float64))[warp] > 0
+
+    for b in range(B):
+        for h in range(H):
+            s = qf[b, h] @ kf[b, h].T
+            if causal:
+                s[rows[None, :] > rows[:, None]] = -np.inf
+            m = np.full(N, -np.inf)
+            for j in range((N + 127) // 128):
+                x = np.full((N, 128), -np.inf)
+                x[:, : min(128, N - 128 * j)] = s[:, 128 * j: 128 * (j + 1)]
+                live = rows >= 128 * j if causal else np.ones(N, bool)
+                with np.errstate(invalid="ignore", over="ignore"):
+                    first = m == -np.inf
+                    s1 = np.where(first, np.inf, np.exp2((x[:, :64] - m[:, None]) * c2).sum(1))
+                    s2 = np.exp2((x[:, 64:] - m[:, None]) * c2).sum(1)
+                full = live & per_warp(live & (s1 > lim))
+                half2 = live & ~full & per_warp(live & ~full & (s2 > lim))
+                counts += [full.sum(), half2.sum(), (live & ~full & ~half2).sum()]
+                m = np.where(full, np.maximum(m, x.max(1)), m)
+                m = np.where(half2 & (s2 > lim), np.maximum(m, x[:, 64:].max(1)), m)
+    return counts

@@ -121,6 +121,26 @@ def test_growing_keys_move_the_reference(dtype, causal):
     parity.assert_within(st, f"growing keys dtype={dtype} causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", [synth.FP16, synth.BF16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_halves_move_the_reference(dtype, d, causal):
+    """Key magnitudes that grow every 64 keys: the weights of a tile's first
+    half may pass against the running reference while those of its second
+    half overflow the bound after the first half went to the tensor core, so
+    U absorbs the first half, is rescaled, and the second half is recomputed
+    (tests/test_softmax_routes.py checks that these inputs take that route)."""
+    q, k, v = parity.keys_growing_by_half(dtype, d)
+    B, H, N, _ = q.shape
+    scale = 1.0 / math.sqrt(d)
+    o, lse, guards = parity.run_gpu(q, k, v, dtype, scale, causal, guard=4096)
+    assert guards, "write outside O or LSE"
+    rows = np.arange(B * H * N, dtype=np.int64)
+    o_ref, lse_ref, spread = parity.oracle_rows(q, k, v, dtype, scale, causal, rows)
+    st = parity.compare(o.reshape(-1, d), lse.reshape(-1), o_ref, lse_ref, spread, dtype)
+    parity.assert_within(st, f"key halves dtype={dtype} d={d} causal={causal}")
+
+
 _INPUTS = {}
 
 
