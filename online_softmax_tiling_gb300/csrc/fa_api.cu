@@ -156,12 +156,18 @@ size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
 // width kd.  Splitting pays for its fp32 partials and merge only when most
 // SMs would otherwise idle: split when the query blocks fill less than half
 // of them, into about one wave of CTAs, keeping at least 512 keys per range.
-int choose_splits(int64_t BH, int Nq, int Nk, int kd) {
-    if (kd == 0) return 1;
+// SMs of the current device (148 if it cannot be asked).
+int sm_count() {
     int device = 0, sms = 148;
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         sms = 148;
+    return sms;
+}
+
+int choose_splits(int64_t BH, int Nq, int Nk, int kd) {
+    if (kd == 0) return 1;
+    const int sms = sm_count();
     const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
     const int64_t ctas = BH * ((Nq + block_m - 1) / block_m);
     if (2 * ctas > sms) return 1;
@@ -246,7 +252,14 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     if (cudaGetDevice(&device) != cudaSuccess) return FA_ERR_CUDA;
     if (!ensure_smem_attr(ke.fn, ke.smem, device)) return FA_ERR_CUDA;
 
+    const int64_t units = BH * nq * num_splits;
     fa::FwdParams prm;
+    prm.o = a.o;
+    prm.o_sb = a.o_stride[0];
+    prm.o_sh = a.o_stride[1];
+    prm.o_sn = a.o_stride[2];
+    prm.d_out = d;
+    prm.num_units = static_cast<int>(units);
     prm.lse = a.lse;
     prm.lse_sb = a.lse_stride[0];
     prm.lse_sh = a.lse_stride[1];
@@ -267,7 +280,9 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
                          : nullptr;
 
     void* args[] = {&tq, &tk, &tv, &to, &prm};
-    const dim3 grid(static_cast<unsigned>(BH * nq * num_splits));
+    // the kernel for d <= 128 is persistent: one CTA per SM walks the units
+    const int64_t ctas = kd <= 128 ? std::min<int64_t>(units, sm_count()) : units;
+    const dim3 grid(static_cast<unsigned>(ctas));
     const dim3 block(static_cast<unsigned>(ke.threads));
     const cudaStream_t st = static_cast<cudaStream_t>(a.stream);
     if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem), st) != cudaSuccess)

@@ -74,6 +74,10 @@ constexpr uint32_t kTmemU = 256;      // U_A at 256, U_B at 384
 __device__ unsigned int g_fa_status;
 
 struct FwdParams {
+    void* o;                  // O row (b, h, row) at o + b o_sb + h o_sh + row o_sn (16-bit elements)
+    long long o_sb, o_sh, o_sn;
+    int d_out;                // columns of O written (the head dim d <= D, a multiple of 8)
+    int num_units;            // query blocks x heads x key ranges
     float* lse;               // LSE of (b, h, row) at lse + b lse_sb + h lse_sh + row
     long long lse_sb, lse_sh;
     int Nq, Nk;               // query rows and keys per (b, h)
@@ -110,6 +114,7 @@ struct Cfg {
 template <int NK, int NV>
 struct alignas(8) Ctl {
     uint64_t q_full;
+    uint64_t q_empty;     // the S products of a unit are done: Q_A, Q_B may be reloaded
     uint64_t k_full[NK];
     uint64_t k_empty[NK];
     uint64_t v_full[NV];
@@ -240,47 +245,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- which rows: consecutive CTAs share a head, so its K/V stay in L2;
-    // with the causal mask the longest query blocks of each head start first.
-    const int split = SPLIT ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
-    const int blk = SPLIT ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
-    const int bh = blk / p.num_q_blocks;
-    int qb = blk % p.num_q_blocks;
-    if (CAUSAL) qb = p.num_q_blocks - 1 - qb;
-    const int b_idx = bh / p.H, h_idx = bh % p.H;
     const int nkv = (p.Nk + kBlockN - 1) / kBlockN;
-    // key tiles visible to query tile A (rows qb*256 + [0,128)) and B ([128,256)):
-    // with the causal mask, up to the tile holding key (last row + offset)
-    auto visible_tiles = [&](int x) {
-        if (!CAUSAL) return nkv;
-        const int last = min(qb * kBlockM + x * kTileM + kTileM - 1, p.Nq - 1) + p.mask_offset;
-        return last < 0 ? 0 : min(last / kBlockN + 1, nkv);
+
+    // ---- work units.  A unit is one query block (two 128-row tiles) of one
+    // (batch, head), and with split-KV one range of its key tiles.  The grid
+    // is persistent: CTA c takes units c, then 2G - 1 - c, 2G + c, ... (G
+    // CTAs; the direction alternates by round, so that with the causal mask,
+    // where units are ordered longest first, every CTA gets a similar share).
+    // Without the mask consecutive units share a head, so its K/V stay in L2.
+    struct Unit {
+        int bh, qb, split, k0, nA, nB;
     };
-    const int T_A = visible_tiles(0);
-    const int T_B = visible_tiles(1);
-    // this CTA visits key tiles k0 .. k0 + n_x - 1 for tile x (all of them
-    // unless split-KV divides the range of the block into num_splits parts)
-    int k0 = 0, nA = T_A, nB = T_B;
-    if constexpr (SPLIT) {
-        const int chunk = (T_B + p.num_splits - 1) / p.num_splits;
-        k0 = split * chunk;
-        const int k1 = min(k0 + chunk, T_B);
-        nB = max(0, k1 - k0);
-        nA = max(0, min(k1, T_A) - k0);
-        if (nB == 0) {  // empty range: its partials carry no weight
-            const int row = qb * kBlockM + static_cast<int>(threadIdx.x);
-            if (threadIdx.x < kBlockM && row < p.Nq) {
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
-                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
-                p.lse_part[i] = -INFINITY;
-                p.lse_part[plane + i] = -INFINITY;
-            }
-            return;
+    const int S = SPLIT ? p.num_splits : 1;
+    auto unit_id = [&](int r) {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        return r * G + ((r & 1) ? G - 1 - c : c);
+    };
+    auto unit_of = [&](int u) {
+        Unit w;
+        if (CAUSAL) {
+            const int per_qb = p.BH * S;
+            w.qb = p.num_q_blocks - 1 - u / per_qb;
+            w.bh = (u % per_qb) / S;
+            w.split = u % S;
+        } else {
+            w.bh = u / (p.num_q_blocks * S);
+            w.qb = (u / S) % p.num_q_blocks;
+            w.split = u % S;
         }
-    }
+        // key tiles visible to query tile A (rows qb*256 + [0,128)) and B
+        // ([128,256)): with the causal mask, up to the tile holding key
+        // (last row + offset)
+        auto visible_tiles = [&](int x) {
+            if (!CAUSAL) return nkv;
+            const int last = min(w.qb * kBlockM + x * kTileM + kTileM - 1, p.Nq - 1) + p.mask_offset;
+            return last < 0 ? 0 : min(last / kBlockN + 1, nkv);
+        };
+        // the unit visits key tiles k0 .. k0 + n_x - 1 for tile x (all of them
+        // unless split-KV divides the range of the block into num_splits parts)
+        const int T_A = visible_tiles(0), T_B = visible_tiles(1);
+        w.k0 = 0;
+        w.nA = T_A;
+        w.nB = T_B;
+        if constexpr (SPLIT) {
+            const int chunk = (T_B + S - 1) / S;
+            w.k0 = w.split * chunk;
+            const int k1 = min(w.k0 + chunk, T_B);
+            w.nB = max(0, k1 - w.k0);
+            w.nA = max(0, min(k1, T_A) - w.k0);
+        }
+        return w;
+    };
 
     const uint32_t bar_q = ptx::smem_addr(&ctl->q_full);
+    const uint32_t bar_qe = ptx::smem_addr(&ctl->q_empty);
     auto bar_kf = [&](int s) { return ptx::smem_addr(&ctl->k_full[s]); };
     auto bar_ke = [&](int s) { return ptx::smem_addr(&ctl->k_empty[s]); };
     auto bar_vf = [&](int s) { return ptx::smem_addr(&ctl->v_full[s]); };
@@ -297,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_q, 1);
+        ptx::mbar_init(bar_qe, 1);
         for (int s = 0; s < NK; ++s) {
             ptx::mbar_init(bar_kf(s), 1);
             ptx::mbar_init(bar_ke(s), 1);
@@ -320,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
-        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
@@ -333,52 +351,68 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kLoaderWarp) {
         // =============================================================== loader
-        // Order K_0, K_1, V_0, K_2, V_1, ...: a K tile is only gated by the
-        // S = Q K^T products that free its slot, never by the slower P.V.
+        // Per unit: Q_A, Q_B once the previous unit's S products are done
+        // (q_empty), then K_0, K_1, V_0, K_2, V_1, ...: a K tile is only gated
+        // by the S = Q K^T products that free its slot, never by the slower
+        // P.V.  The rings run on across units, so the first tiles of a unit
+        // load while the previous one finishes.
         int issued_k[NK], issued_v[NV];
 #pragma unroll
         for (int s = 0; s < NK; ++s) issued_k[s] = 0;
 #pragma unroll
         for (int s = 0; s < NV; ++s) issued_v[s] = 0;
-        if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+        uint32_t kc = 0, vc = 0;  // K and V tiles loaded so far
+        int nq = 0;               // units whose Q was loaded
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            if (w.nB == 0) continue;
+            const int b_idx = w.bh / p.H, h_idx = w.bh % p.H;
+            if (nq > 0 && !(ok = wait_warp(bar_qe, (nq - 1) & 1, abort, tmo))) break;
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
 #pragma unroll
-            for (int x = 0; x < 2; ++x)
-#pragma unroll
-                for (int c = 0; c < C::kSub; ++c)
-                    ptx::tma_load_4d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
-                                     qb * kBlockM + x * kTileM, h_idx, b_idx);
-        }
-        for (int j = 0; j <= nB; ++j) {
-            if (j < nB) {
-                const int s = j % NK;
-                if (j >= NK && !wait_warp(bar_ke(s), ((j / NK) - 1) & 1, abort, tmo)) break;
-                const bool skip = (p.fault_mode == 1 && j == 0);
-                if (lane == 0 && !skip) {
-                    ptx::mbar_arrive_expect_tx(bar_kf(s), C::kTileBytes);
+                for (int x = 0; x < 2; ++x)
 #pragma unroll
                     for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sK(s) + c * kSubBytes, &tm_k, bar_kf(s), 64 * c,
-                                         (k0 + j) * kBlockN, h_idx, b_idx);
-                }
-                if (!skip) ++issued_k[s];
+                        ptx::tma_load_4d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
+                                         w.qb * kBlockM + x * kTileM, h_idx, b_idx);
             }
-            if (j >= 1) {
-                const int jv = j - 1;
-                const int s = jv % NV;
-                if (jv >= NV && !wait_warp(bar_ve(s), ((jv / NV) - 1) & 1, abort, tmo)) break;
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar_vf(s), C::kTileBytes);
+            ++nq;
+            for (int j = 0; j <= w.nB; ++j) {
+                if (j < w.nB) {
+                    const int s = kc % NK;
+                    if (kc >= NK && !(ok = wait_warp(bar_ke(s), ((kc / NK) - 1) & 1, abort, tmo))) break;
+                    const bool skip = (p.fault_mode == 1 && kc == 0);
+                    if (lane == 0 && !skip) {
+                        ptx::mbar_arrive_expect_tx(bar_kf(s), C::kTileBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sV(s) + c * kSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                         (k0 + jv) * kBlockN, h_idx, b_idx);
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sK(s) + c * kSubBytes, &tm_k, bar_kf(s), 64 * c,
+                                             (w.k0 + j) * kBlockN, h_idx, b_idx);
+                    }
+                    if (!skip) ++issued_k[s];
+                    ++kc;
                 }
-                ++issued_v[s];
+                if (j >= 1) {
+                    const int s = vc % NV;
+                    if (vc >= NV && !(ok = wait_warp(bar_ve(s), ((vc / NV) - 1) & 1, abort, tmo))) break;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar_vf(s), C::kTileBytes);
+#pragma unroll
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sV(s) + c * kSubBytes, &tm_v, bar_vf(s), 64 * c,
+                                             (w.k0 + j - 1) * kBlockN, h_idx, b_idx);
+                    }
+                    ++issued_v[s];
+                    ++vc;
+                }
             }
         }
         // Never leave the CTA with copies still landing in its shared memory.
-        wait_warp(bar_q, 0, abort, tmo, false);
+        if (nq > 0) wait_warp(bar_q, (nq - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NK; ++s)
             if (issued_k[s] > 0) wait_warp(bar_kf(s), (issued_k[s] - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NV; ++s)
@@ -409,57 +443,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_ts_k64(tmem + kTmemU + x * 128, tmem + x * 128 + half * 32,
                             v_desc0 + s * kTileStep + half * 512, idesc_pv, acc ? 1u : 0u);
         };
-        // both halves of P_x(j) V_j, each issued once the softmax warps have
-        // written its weights; o_half / o_ready signal that U_x absorbed them
-        auto pv_tile = [&](int x, int s, int j) {
-            if (!wait_warp(bar_ph(x), j & 1, abort, tmo)) return false;
+        // both halves of P_x V_s for the n-th key tile of query tile x, each
+        // issued once the softmax warps have written its weights; o_half /
+        // o_ready signal that U_x absorbed them
+        auto pv_tile = [&](int x, int s, uint32_t n, bool acc) {
+            if (!wait_warp(bar_ph(x), n & 1, abort, tmo)) return false;
             ptx::tc_fence_after_sync();
-            issue_pv(x, s, 0, j > 0);
+            issue_pv(x, s, 0, acc);
             ptx::tc_commit_elect(bar_oh(x));
-            if (!wait_warp(bar_pf(x), j & 1, abort, tmo)) return false;
+            if (!wait_warp(bar_pf(x), n & 1, abort, tmo)) return false;
             ptx::tc_fence_after_sync();
             issue_pv(x, s, 1, true);
             ptx::tc_commit_elect(bar_o(x));
             return true;
         };
-        bool ok = nB > 0 && wait_warp(bar_q, 0, abort, tmo) && wait_warp(bar_kf(0), 0, abort, tmo);
-        if (ok) {
-            ptx::tc_fence_after_sync();
-            if (nA > 0) {
-                issue_s(0, 0);
-                ptx::tc_commit_elect(bar_sf(0));
-            }
-            issue_s(1, 0);
-            ptx::tc_commit_elect(bar_sf(1));
-            ptx::tc_commit_elect(bar_ke(0));
-            __syncwarp();
-        }
-        for (int j = 0; ok && j < nB; ++j) {
-            const int sv = j % NV;
-            const int sk = (j + 1) % NK;
-            bool k_ready = false;
-            if (!(ok = wait_warp(bar_vf(sv), (j / NV) & 1, abort, tmo))) break;
-            if (j < nA) {
-                if (!(ok = pv_tile(0, sv, j))) break;
-                if (j + 1 < nA) {
-                    if (!(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
-                    k_ready = true;
-                    ptx::tc_fence_after_sync();
-                    issue_s(0, sk);
+        uint32_t kc = 0, vc = 0;    // K and V tiles consumed so far (same order as loaded)
+        uint32_t na = 0, nb = 0;    // key tiles of query tile A and B so far
+        uint32_t nq = 0;            // units so far (q_full phase)
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            if (w.nB == 0) continue;
+            if (!(ok = wait_warp(bar_q, nq & 1, abort, tmo))) break;
+            ++nq;
+            {
+                const int s0 = kc % NK;
+                if (!(ok = wait_warp(bar_kf(s0), (kc / NK) & 1, abort, tmo))) break;
+                ptx::tc_fence_after_sync();
+                // S_x(0) overwrites columns the softmax warps finished with
+                // when they signalled the last P of the previous unit
+                if (w.nA > 0) {
+                    issue_s(0, s0);
                     ptx::tc_commit_elect(bar_sf(0));
                 }
+                issue_s(1, s0);
+                ptx::tc_commit_elect(bar_sf(1));
+                ptx::tc_commit_elect(bar_ke(s0));
+                if (w.nB == 1) ptx::tc_commit_elect(bar_qe);  // Q_A, Q_B read for the last time
+                ++kc;
                 __syncwarp();
             }
-            if (!(ok = pv_tile(1, sv, j))) break;
-            if (j + 1 < nB) {
-                if (!k_ready && !(ok = wait_warp(bar_kf(sk), ((j + 1) / NK) & 1, abort, tmo))) break;
-                ptx::tc_fence_after_sync();
-                issue_s(1, sk);
-                ptx::tc_commit_elect(bar_sf(1));
-                ptx::tc_commit_elect(bar_ke(sk));
+            for (int j = 0; j < w.nB; ++j) {
+                const int sv = vc % NV;
+                const int sk = kc % NK;
+                bool k_ready = false;
+                if (!(ok = wait_warp(bar_vf(sv), (vc / NV) & 1, abort, tmo))) break;
+                if (j < w.nA) {
+                    // the first product of a unit overwrites U_x; the softmax
+                    // warps read the previous unit's U_x before they signal P
+                    if (!(ok = pv_tile(0, sv, na, j > 0))) break;
+                    ++na;
+                    if (j + 1 < w.nA) {
+                        if (!(ok = wait_warp(bar_kf(sk), (kc / NK) & 1, abort, tmo))) break;
+                        k_ready = true;
+                        ptx::tc_fence_after_sync();
+                        issue_s(0, sk);
+                        ptx::tc_commit_elect(bar_sf(0));
+                    }
+                    __syncwarp();
+                }
+                if (!(ok = pv_tile(1, sv, nb, j > 0))) break;
+                ++nb;
+                if (j + 1 < w.nB) {
+                    if (!k_ready && !(ok = wait_warp(bar_kf(sk), (kc / NK) & 1, abort, tmo))) break;
+                    ptx::tc_fence_after_sync();
+                    issue_s(1, sk);
+                    ptx::tc_commit_elect(bar_sf(1));
+                    ptx::tc_commit_elect(bar_ke(sk));
+                    if (j + 2 == w.nB) ptx::tc_commit_elect(bar_qe);
+                    ++kc;
+                }
+                ptx::tc_commit_elect(bar_ve(sv));
+                ++vc;
+                __syncwarp();
             }
-            ptx::tc_commit_elect(bar_ve(sv));
-            __syncwarp();
         }
         // Drain: nothing of ours may still run on the tensor core at teardown.
         ptx::tc_commit_elect(bar_drain);
@@ -469,8 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ======================================== softmax + epilogue of tile x
         const int x = warp >> 2;                          // 0: tile A, 1: tile B
         const int t = threadIdx.x & 127;                  // row in the tile = TMEM lane
-        const int row = qb * kBlockM + x * kTileM + t;    // query index in the head
-        const int T = x == 0 ? nA : nB;          // key tiles this CTA visits for the tile
+        // of the current unit: this thread's query index in the head, the
+        // tile's first one, the first key tile and how many are visited
+        int row = 0, first_row = 0, k0 = 0, T = 0;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + x * 128;
         const uint32_t u_addr = tmem + lane_off + kTmemU + x * 128;
@@ -479,7 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whether key tile j (local index) holds a key some row of this tile
         // may not see: keys >= Nk, or keys past the causal limit of the tile's
         // first row (with a bottom-right offset that can be two tiles)
-        const int first_row = qb * kBlockM + x * kTileM;
         auto tile_masked = [&](int j) {
             const int kend = (k0 + j + 1) * kBlockN;
             return kend > p.Nk || (CAUSAL && kend - 1 > first_row + p.mask_offset);
@@ -535,175 +594,194 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (u >= limit) sv[u] = __float_as_uint(-INFINITY);
             }
         };
-        float m_ref = -INFINITY;              // reference maximum of the raw scores
-        float2 lsum = make_float2(0.f, 0.f);  // sum of the fp32 weights (for LSE) in .x
-        float2 lhat = make_float2(0.f, 0.f);  // sum of the 16-bit weights fed to P.V (for O) in .x
+        uint32_t n = 0;  // key tiles of this query tile so far, over all units (barrier phases)
         bool aborted = false;
+        for (int r = 0; !aborted; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            const int b_idx = w.bh / p.H, h_idx = w.bh % p.H;
+            first_row = w.qb * kBlockM + x * kTileM;
+            row = first_row + t;
+            k0 = w.k0;
+            T = x == 0 ? w.nA : w.nB;
+            if (SPLIT && w.nB == 0) {  // empty key range: its partials carry no weight
+                if (row < p.Nq) {
+                    const size_t i = (static_cast<size_t>(w.split) * p.BH + w.bh) * p.Nq + row;
+                    const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
+                    p.lse_part[i] = -INFINITY;
+                    p.lse_part[plane + i] = -INFINITY;
+                }
+                continue;
+            }
+            float m_ref = -INFINITY;              // reference maximum of the raw scores
+            float2 lsum = make_float2(0.f, 0.f);  // sum of the fp32 weights (for LSE) in .x
+            float2 lhat = make_float2(0.f, 0.f);  // sum of the 16-bit weights fed to P.V (for O) in .x
 
-        for (int j = 0; j < T; ++j) {
-            if (!wait_warp(bar_sf(x), j & 1, abort, tmo)) {
-                aborted = true;
-                break;
-            }
-            ptx::tc_fence_after_sync();
-            // keys 0-63 of tile j-1 are in U_x (S_x(j) was issued after them);
-            // taking that phase here keeps a later wait on phase j unambiguous
-            if (j > 0 && !wait_warp(bar_oh(x), (j - 1) & 1, abort, tmo)) {
-                aborted = true;
-                break;
-            }
-            // common case: weights against the current reference, checked by
-            // their sum before they are written, one 64-key half at a time: the
-            // first half goes to the tensor core while the second is computed.
-            // The first tile (no reference yet) or a first half above the bound
-            // takes the tile maximum and recomputes all weights from the scores
-            // still in TMEM; a second half above the bound moves the reference
-            // for that half only (all branches warp-uniform).
-            uint32_t pk[kBlockN / 2];
-            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // keys 64-127 (or all)
-            float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            float r1 = 0.f, h1 = 0.f;  // sums of keys 0-63 when they were sent on the old reference
-            // (tcgen05.ld is warp-collective: every branch around it is uniform)
-            bool redo = (m_ref == -INFINITY);
-            bool half_sent = false;
-            float alpha = 1.f;
-            float m_new = m_ref;
-            if (!__any_sync(0xffffffffu, redo)) {
-                uint32_t sv[kBlockN];
-                load_scores(sv, j);
-                float2 s1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                float2 t1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                weights(sv, kBlockN / 4, -m_ref * c2, pk, s1, t1);
-                r1 = s1[0].x + s1[0].y + s1[1].x + s1[1].y;
-                redo = r1 > weight_sum_limit<BF16>();
+            for (int j = 0; j < T; ++j, ++n) {
+                if (!wait_warp(bar_sf(x), n & 1, abort, tmo)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                // keys 0-63 of the previous key tile are in U_x (S_x(j) was issued
+                // after them); taking that phase here keeps a later wait on this
+                // tile's phase unambiguous
+                if (j > 0 && !wait_warp(bar_oh(x), (n - 1) & 1, abort, tmo)) {
+                    aborted = true;
+                    break;
+                }
+                // common case: weights against the current reference, checked by
+                // their sum before they are written, one 64-key half at a time: the
+                // first half goes to the tensor core while the second is computed.
+                // The first tile (no reference yet) or a first half above the bound
+                // takes the tile maximum and recomputes all weights from the scores
+                // still in TMEM; a second half above the bound moves the reference
+                // for that half only (all branches warp-uniform).
+                uint32_t pk[kBlockN / 2];
+                float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // keys 64-127 (or all)
+                float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float r1 = 0.f, h1 = 0.f;  // sums of keys 0-63 when they were sent on the old reference
+                // (tcgen05.ld is warp-collective: every branch around it is uniform)
+                bool redo = (m_ref == -INFINITY);
+                bool half_sent = false;
+                float alpha = 1.f;
+                float m_new = m_ref;
                 if (!__any_sync(0xffffffffu, redo)) {
+                    uint32_t sv[kBlockN];
+                    load_scores(sv, j);
+                    float2 s1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 t1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    weights(sv, kBlockN / 4, -m_ref * c2, pk, s1, t1);
+                    r1 = s1[0].x + s1[0].y + s1[1].x + s1[1].y;
+                    redo = r1 > weight_sum_limit<BF16>();
+                    if (!__any_sync(0xffffffffu, redo)) {
+                        ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                        ptx::tmem_wait_st();
+                        ptx::tc_fence_before_sync();
+                        ptx::mbar_arrive(bar_ph(x));
+                        half_sent = true;
+                        const float2 h = __fadd2_rn(t1[0], t1[1]);
+                        h1 = h.x + h.y;
+                        weights(sv + kBlockN / 2, kBlockN / 4, -m_ref * c2, pk + kBlockN / 4, rs, rh);
+                        const bool redo2 =
+                            rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
+                        if (__any_sync(0xffffffffu, redo2)) {
+                            float mt = -INFINITY;
+#pragma unroll 1
+                            for (int c = 2; c < kBlockN / 32; ++c) {
+                                uint32_t sc[32];
+                                load_chunk(sc, c, j);
+#pragma unroll
+                                for (int u = 0; u < 32; u += 2)
+                                    mt = ptx::fmax3(mt, __uint_as_float(sc[u]), __uint_as_float(sc[u + 1]));
+                            }
+                            if (redo2) {
+                                m_new = fmaxf(mt, m_ref);
+                                alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                            }
+                            rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int c = 2; c < kBlockN / 32; ++c) {
+                                uint32_t sc[32];
+                                load_chunk(sc, c, j);
+                                weights(sc, 16, -m_new * c2, &pk[16 * c], rs, rh);
+                            }
+                        }
+                    } else {
+                        r1 = 0.f;
+                    }
+                }
+                if (!half_sent) {
+                    float mt = -INFINITY;
+#pragma unroll 1
+                    for (int c = 0; c < kBlockN / 32; ++c) {
+                        uint32_t sv[32];
+                        load_chunk(sv, c, j);
+                        float mx[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
+#pragma unroll
+                        for (int u = 4; u + 8 <= 32; u += 8)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
+                                                   __uint_as_float(sv[u + 4 + w]));
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
+                        mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    }
+                    // every lane takes the tile maximum: a lane whose first half
+                    // was in range may still overflow in its second half, which
+                    // was never checked (alpha is exactly 1 where m does not move)
+                    m_new = fmaxf(mt, m_ref);
+                    if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                    // a row with no valid key so far keeps all weights at zero
+                    const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 32; ++c) {
+                        uint32_t sv[32];
+                        load_chunk(sv, c, j);
+                        weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
+                    }
                     ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-                    ptx::tmem_wait_st();
-                    ptx::tc_fence_before_sync();
-                    ptx::mbar_arrive(bar_ph(x));
-                    half_sent = true;
-                    const float2 h = __fadd2_rn(t1[0], t1[1]);
-                    h1 = h.x + h.y;
-                    weights(sv + kBlockN / 2, kBlockN / 4, -m_ref * c2, pk + kBlockN / 4, rs, rh);
-                    const bool redo2 =
-                        rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
-                    if (__any_sync(0xffffffffu, redo2)) {
-                        float mt = -INFINITY;
-#pragma unroll 1
-                        for (int c = 2; c < kBlockN / 32; ++c) {
-                            uint32_t sc[32];
-                            load_chunk(sc, c, j);
-#pragma unroll
-                            for (int u = 0; u < 32; u += 2)
-                                mt = ptx::fmax3(mt, __uint_as_float(sc[u]), __uint_as_float(sc[u + 1]));
+                }
+                // l = alpha (l + keys sent on the old reference) + the rest
+                const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
+                lsum.x = fmaf(lsum.x + r1, alpha, r.x + r.y);
+                lhat.x = fmaf(lhat.x + h1, alpha, hh.x + hh.y);
+                ptx::tmem_st_32x32b_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                // U_x holds P(j-1) V, since S_x(j) was issued after that product.
+                // Rescale it by alpha when the reference maximum moved (warp-uniform);
+                // if keys 0-63 of this tile were already sent, U_x must absorb them
+                // first: they carry the old reference too.
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    if (half_sent) {
+                        if (!wait_warp(bar_oh(x), n & 1, abort, tmo)) {
+                            aborted = true;
+                            break;
                         }
-                        if (redo2) {
-                            m_new = fmaxf(mt, m_ref);
-                            alpha = ptx::ex2_approx((m_ref - m_new) * c2);
-                        }
-                        rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int c = 2; c < kBlockN / 32; ++c) {
-                            uint32_t sc[32];
-                            load_chunk(sc, c, j);
-                            weights(sc, 16, -m_new * c2, &pk[16 * c], rs, rh);
-                        }
+                        ptx::tc_fence_after_sync();
                     }
-                } else {
-                    r1 = 0.f;
-                }
-            }
-            if (!half_sent) {
-                float mt = -INFINITY;
+                    const float2 av = make_float2(alpha, alpha);
 #pragma unroll 1
-                for (int c = 0; c < kBlockN / 32; ++c) {
-                    uint32_t sv[32];
-                    load_chunk(sv, c, j);
-                    float mx[4];
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t ov[16];
+                        ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
-#pragma unroll
-                    for (int u = 4; u + 8 <= 32; u += 8)
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
-                                               __uint_as_float(sv[u + 4 + w]));
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
-                    mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                }
-                // every lane takes the tile maximum: a lane whose first half
-                // was in range may still overflow in its second half, which
-                // was never checked (alpha is exactly 1 where m does not move)
-                m_new = fmaxf(mt, m_ref);
-                if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
-                // a row with no valid key so far keeps all weights at zero
-                const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) {
-                    uint32_t sv[32];
-                    load_chunk(sv, c, j);
-                    weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
-                }
-                ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-            }
-            // l = alpha (l + keys sent on the old reference) + the rest
-            const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
-            lsum.x = fmaf(lsum.x + r1, alpha, r.x + r.y);
-            lhat.x = fmaf(lhat.x + h1, alpha, hh.x + hh.y);
-            ptx::tmem_st_32x32b_x32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-            // U_x holds P(j-1) V, since S_x(j) was issued after that product.
-            // Rescale it by alpha when the reference maximum moved (warp-uniform);
-            // if keys 0-63 of this tile were already sent, U_x must absorb them
-            // first: they carry the old reference too.
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                if (half_sent) {
-                    if (!wait_warp(bar_oh(x), j & 1, abort, tmo)) {
-                        aborted = true;
-                        break;
+                        for (int u = 0; u < 16; u += 2) {
+                            ptx::reg_fence(ov[u]);
+                            ptx::reg_fence(ov[u + 1]);
+                            const float2 r = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), av);
+                            ov[u] = __float_as_uint(r.x);
+                            ov[u + 1] = __float_as_uint(r.y);
+                        }
+                        ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
                     }
-                    ptx::tc_fence_after_sync();
                 }
-                const float2 av = make_float2(alpha, alpha);
-#pragma unroll 1
-                for (int c = 0; c < D / 16; ++c) {
-                    uint32_t ov[16];
-                    ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
-                        ptx::reg_fence(ov[u]);
-                        ptx::reg_fence(ov[u + 1]);
-                        const float2 r = __fmul2_rn(
-                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), av);
-                        ov[u] = __float_as_uint(r.x);
-                        ov[u + 1] = __float_as_uint(r.y);
-                    }
-                    ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
-                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                if (!half_sent) ptx::mbar_arrive(bar_ph(x));
+                ptx::mbar_arrive(bar_pf(x));
+                m_ref = m_new;
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before_sync();
-            if (!half_sent) ptx::mbar_arrive(bar_ph(x));
-            ptx::mbar_arrive(bar_pf(x));
-            m_ref = m_new;
-        }
 
-        // ---- epilogue: O = U / lhat -> 16-bit -> swizzled smem -> TMA store
-        if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (T - 1) & 1, abort, tmo);
-        // a tile that sees no key stages its zeros over the Q tile: wait until
-        // the copy of Q has landed, or it could overwrite them
-        if (!SPLIT && !aborted && T == 0) aborted = !wait_warp(bar_q, 0, abort, tmo);
-        const float l_all = lsum.x + lsum.y;
-        const float lhat_all = lhat.x + lhat.y;
-        if constexpr (SPLIT) {
-            // partial result of this key range: O normalised by its own lhat
-            // (fp32) and the two log-sums that weight it in the merge
-            // (warp-uniform branches around the collective tcgen05.ld)
-            if (!aborted) {
+            // ---- epilogue: O = U / lhat -> 16-bit, stored from registers (each
+            // thread its own row), so that Q's shared memory is free for the
+            // next unit as soon as its last S product is done
+            if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (n - 1) & 1, abort, tmo);
+            if (aborted) break;
+            const float l_all = lsum.x + lsum.y;
+            const float lhat_all = lhat.x + lhat.y;
+            if constexpr (SPLIT) {
+                // partial result of this key range: O normalised by its own lhat
+                // (fp32) and the two log-sums that weight it in the merge
+                // (warp-uniform branches around the collective tcgen05.ld)
                 const bool mine = row < p.Nq && !*abort;
                 const bool any = T > 0 && l_all > 0.f;
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (mine ? row : 0);
+                const size_t i = (static_cast<size_t>(w.split) * p.BH + w.bh) * p.Nq + (mine ? row : 0);
                 const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
                 if (mine) {
                     p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
@@ -719,71 +797,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
                         ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int u = 0; u < 32; u += 4) {
-                            ptx::reg_fence(ov[u]);
-                            ptx::reg_fence(ov[u + 1]);
-                            ptx::reg_fence(ov[u + 2]);
-                            ptx::reg_fence(ov[u + 3]);
+                        for (int e = 0; e < 32; e += 4) {
+                            ptx::reg_fence(ov[e]);
+                            ptx::reg_fence(ov[e + 1]);
+                            ptx::reg_fence(ov[e + 2]);
+                            ptx::reg_fence(ov[e + 3]);
                             if (mine)
-                                dst[c * 8 + u / 4] = make_float4(
-                                    __uint_as_float(ov[u]) * inv, __uint_as_float(ov[u + 1]) * inv,
-                                    __uint_as_float(ov[u + 2]) * inv, __uint_as_float(ov[u + 3]) * inv);
+                                dst[c * 8 + e / 4] = make_float4(
+                                    __uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                    __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
                         }
                     }
                 }
-            }
-        } else if (!aborted) {
-            ptx::tc_fence_after_sync();
-            const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
-            const float2 iv = make_float2(inv, inv);
+            } else {
+                ptx::tc_fence_after_sync();
+                const bool mine = row < p.Nq && !*abort;
+                const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
+                const float2 iv = make_float2(inv, inv);
+                uint16_t* orow = static_cast<uint16_t*>(p.o) + b_idx * p.o_sb + h_idx * p.o_sh +
+                                 static_cast<long long>(mine ? row : 0) * p.o_sn;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                if (T > 0) {
-                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
-                    ptx::tmem_wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    if (T > 0) {
+                        ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) ptx::reg_fence(ov[u]);
-                } else {  // no key visible to this tile: O = 0 (U was never written)
+                        for (int e = 0; e < 32; ++e) ptx::reg_fence(ov[e]);
+                    } else {  // no key visible to this tile: O = 0 (U was not written)
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) ov[u] = 0u;
-                }
-                // the Q tile's shared memory is free now (all S_x products are
-                // done) and becomes the staging buffer, in the 128-byte-swizzled
-                // layout the TMA store expects
-                const uint32_t sub = sQ(x) + (c >> 1) * kSubBytes + t * 128;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = (c & 1) * 4 + q4;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int u = q4 * 8 + 2 * e;
-                        const float2 o2 = __fmul2_rn(
-                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), iv);
-                        w[e] = pack2<BF16>(o2.x, o2.y);
+                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
                     }
-                    const uint32_t dst = sub + ((chunk ^ (t & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]),
-                                 "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                 : "memory");
+                    // 8 columns (16 bytes) per store; columns >= d are not written
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c8 = q4 * 8 + 2 * e;
+                            const float2 o2 = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[c8]), __uint_as_float(ov[c8 + 1])), iv);
+                            wv[e] = pack2<BF16>(o2.x, o2.y);
+                        }
+                        const int col = c * 32 + q4 * 8;
+                        if (mine && col < p.d_out)
+                            *reinterpret_cast<uint4*>(orow + col) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    }
+                }
+                if (mine) {
+                    const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
+                    p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
                 }
             }
-            ptx::fence_proxy_async_smem();
-        }
-        ptx::named_barrier_sync(1 + x, kTileM);
-        if (!SPLIT && t == 0 && !*abort) {
-#pragma unroll
-            for (int c = 0; c < C::kSub; ++c)
-                ptx::tma_store_4d(&tm_o, sQ(x) + c * kSubBytes, 64 * c, qb * kBlockM + x * kTileM,
-                                  h_idx, b_idx);
-            ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read0();
-        }
-        if (!SPLIT && !aborted && !*abort && row < p.Nq) {
-            const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
-            p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
-        }
+        }  // units
     }
 
     // ---- teardown: every tcgen05 op of this CTA has completed
