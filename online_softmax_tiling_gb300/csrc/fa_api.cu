@@ -245,7 +245,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride, qrows) ||
         !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride, krows) ||
         !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride, krows) ||
-        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, qrows))
+        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, kd <= 128 ? 32u : qrows))
         return FA_ERR_CUDA;
 
     int device = 0;
@@ -254,11 +254,6 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
 
     const int64_t units = BH * nq * num_splits;
     fa::FwdParams prm;
-    prm.o = a.o;
-    prm.o_sb = a.o_stride[0];
-    prm.o_sh = a.o_stride[1];
-    prm.o_sn = a.o_stride[2];
-    prm.d_out = d;
     prm.num_units = static_cast<int>(units);
     prm.lse = a.lse;
     prm.lse_sb = a.lse_stride[0];

@@ -74,9 +74,6 @@ constexpr uint32_t kTmemU = 256;      // U_A at 256, U_B at 384
 __device__ unsigned int g_fa_status;
 
 struct FwdParams {
-    void* o;                  // O row (b, h, row) at o + b o_sb + h o_sh + row o_sn (16-bit elements)
-    long long o_sb, o_sh, o_sn;
-    int d_out;                // columns of O written (the head dim d <= D, a multiple of 8)
     int num_units;            // query blocks x heads x key ranges
     float* lse;               // LSE of (b, h, row) at lse + b lse_sb + h lse_sh + row
     long long lse_sb, lse_sh;
@@ -107,7 +104,10 @@ struct Cfg {
     static constexpr int kOffQ = 0;                      // Q_A, Q_B
     static constexpr int kOffK = 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-    static constexpr int kOffCtl = kOffV + kVStages * kTileBytes;
+    // O staging: one 32-row x 64-column swizzled box per softmax warp
+    static constexpr int kOffStage = kOffV + kVStages * kTileBytes;
+    static constexpr int kStageBytes = 32 * 128;
+    static constexpr int kOffCtl = kOffStage + 8 * kStageBytes;
     static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
 };
 
@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
@@ -810,38 +811,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
+                // each warp stores its 32 rows, 64 columns at a time, through
+                // its own staging box (the 128-byte-swizzled layout the TMA
+                // store expects); rows >= Nq and columns >= d are clipped
                 ptx::tc_fence_after_sync();
                 const bool mine = row < p.Nq && !*abort;
                 const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
                 const float2 iv = make_float2(inv, inv);
-                uint16_t* orow = static_cast<uint16_t*>(p.o) + b_idx * p.o_sb + h_idx * p.o_sh +
-                                 static_cast<long long>(mine ? row : 0) * p.o_sn;
+                const uint32_t stage = sbase + C::kOffStage + warp * C::kStageBytes;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    if (T > 0) {
-                        ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
-                        ptx::tmem_wait_ld();
+                for (int h = 0; h < C::kSub; ++h) {
+                    // the previous store from this box has read it
+                    if (lane == 0) ptx::bulk_wait_group_read0();
+                    __syncwarp();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ptx::reg_fence(ov[e]);
-                    } else {  // no key visible to this tile: O = 0 (U was not written)
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t ov[32];
+                        if (T > 0) {
+                            ptx::tmem_ld_32x32b_x32(u_addr + (2 * h + cc) * 32, ov);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
-                    }
-                    // 8 columns (16 bytes) per store; columns >= d are not written
+                            for (int e = 0; e < 32; ++e) ptx::reg_fence(ov[e]);
+                        } else {  // no key visible to this tile: O = 0 (U was not written)
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t wv[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c8 = q4 * 8 + 2 * e;
-                            const float2 o2 = __fmul2_rn(
-                                make_float2(__uint_as_float(ov[c8]), __uint_as_float(ov[c8 + 1])), iv);
-                            wv[e] = pack2<BF16>(o2.x, o2.y);
+                            for (int e = 0; e < 32; ++e) ov[e] = 0u;
                         }
-                        const int col = c * 32 + q4 * 8;
-                        if (mine && col < p.d_out)
-                            *reinterpret_cast<uint4*>(orow + col) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c8 = q4 * 8 + 2 * e;
+                                const float2 o2 = __fmul2_rn(
+                                    make_float2(__uint_as_float(ov[c8]), __uint_as_float(ov[c8 + 1])), iv);
+                                wv[e] = pack2<BF16>(o2.x, o2.y);
+                            }
+                            const uint32_t dst = stage + lane * 128 + (((cc * 4 + q4) ^ (lane & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(wv[0]),
+                                         "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                                         : "memory");
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && !*abort) {
+                        ptx::tma_store_4d(&tm_o, stage, 64 * h, first_row + 32 * (warp & 3), h_idx, b_idx);
+                        ptx::bulk_commit_group();
                     }
                 }
                 if (mine) {
@@ -850,6 +865,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }  // units
+        // the CTA's shared memory must outlive the stores that read it
+        if (lane == 0) ptx::bulk_wait_group0();
     }
 
     // ---- teardown: every tcgen05 op of this CTA has completed
