@@ -245,7 +245,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride, qrows) ||
         !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride, krows) ||
         !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride, krows) ||
-        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, kd <= 128 ? 32u : qrows))
+        !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, 32u))  // one warp's rows per store
         return FA_ERR_CUDA;
 
     int device = 0;
@@ -275,8 +275,8 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
                          : nullptr;
 
     void* args[] = {&tq, &tk, &tv, &to, &prm};
-    // the kernel for d <= 128 is persistent: one CTA per SM walks the units
-    const int64_t ctas = kd <= 128 ? std::min<int64_t>(units, sm_count()) : units;
+    // the kernels are persistent: one CTA per SM walks the units
+    const int64_t ctas = std::min<int64_t>(units, sm_count());
     const dim3 grid(static_cast<unsigned>(ctas));
     const dim3 block(static_cast<unsigned>(ke.threads));
     const cudaStream_t st = static_cast<cudaStream_t>(a.stream);

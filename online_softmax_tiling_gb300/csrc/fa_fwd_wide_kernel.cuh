@@ -9,9 +9,12 @@
 // the tiling, because a wide head does not fit the two-query-tile layout:
 // two tiles would need 2 x (128 + d) TMEM columns, more than the 512 an SM has.
 //
-//   * one CTA per 128-row query tile; 6 warps: warps 0-3 softmax + epilogue
-//     (thread t owns row t = TMEM lane t), warp 4 the TMA loader, warp 5 the
-//     tensor-core issuer;
+//   * a persistent grid: each CTA walks units of one 128-row query tile of
+//     one (batch, head) (and with split-KV one key range of it), in the
+//     order of fa_fwd_kernel (longest first with the causal mask, the
+//     direction alternating by round); 6 warps: warps 0-3 softmax +
+//     epilogue (thread t owns row t = TMEM lane t), warp 4 the TMA loader,
+//     warp 5 the tensor-core issuer;
 //   * key tiles of 128 keys, so that S = Q K^T runs as M128 N128 products
 //     (an N64 product takes 48 cycles for 32 cycles of work); K and V tiles
 //     of 128 x d fit once each in shared memory next to Q for d = 256 (K
@@ -19,20 +22,27 @@
 //     first use runs;
 //   * TMEM: two score buffers S0 at column 0 and S1 at 128 (128 fp32
 //     columns; the weights P overwrite the first 64), U at column 256 (d
-//     columns);
-//   * tensor-core order: S(0), S(1), then per key tile j: PV(j), S(j+2).
-//     The softmax of tile j+1 runs while the tensor core computes PV(j) and
-//     S(j+2) - with d = 256 each is 1024 cycles, so the softmax of 128 keys
-//     (about 1200 cycles) stays off the critical path.
+//     columns).  Key tiles are counted over all units of the CTA; tile g
+//     uses buffer g & 1, so the buffers, rings and barrier phases run on
+//     from one unit to the next;
+//   * tensor-core order per unit: S(0), S(1), then per key tile j: PV(j),
+//     S(j+2).  The softmax of tile j+1 runs while the tensor core computes
+//     PV(j) and S(j+2) - with d = 256 each is 1024 cycles, so the softmax of
+//     128 keys (about 1200 cycles) stays off the critical path.  The next
+//     unit's Q is loaded once this unit's last S product is done, and its
+//     first two S products follow this unit's last PV;
 //   * S(j+1) is issued before PV(j), so U may still be absorbing P(j-1) V
 //     when the softmax of tile j wants to rescale it: that (rare) rescale
 //     first waits for PV(j-1).  Each score buffer has its own "weights
 //     written" barrier, because the softmax can run one tile ahead of the
-//     issuer's wait; and "U has absorbed P(j) V" alternates between two
-//     barriers by the parity of j: when a softmax warp finishes its last
-//     tile n-1, PV(n-3) is certain to be complete but PV(n-2) is not, so a
-//     single barrier could be two phases behind the one awaited, and a
-//     parity wait cannot tell two phases apart.
+//     issuer's wait; and "U has absorbed P(g) V" alternates between two
+//     barriers by the parity of g: when a softmax warp finishes tile g,
+//     PV(g-2) is certain to be complete but PV(g-1) is not, so a single
+//     barrier could be two phases behind the one awaited, and a parity wait
+//     cannot tell two phases apart;
+//   * O leaves through two 4 KB staging boxes per softmax warp (32 rows x 64
+//     columns, 128-byte swizzle) and TMA stores, never through Q's shared
+//     memory, which the next unit's Q may already occupy.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"
@@ -58,20 +68,24 @@ struct WideCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
-    static constexpr int kOffCtl = kOffV + kVStages * kKVBytes;
+    // O staging: two 32-row x 64-column swizzled boxes per softmax warp
+    static constexpr int kOffStage = kOffV + kVStages * kKVBytes;
+    static constexpr int kStageBytes = 32 * 128;
+    static constexpr int kOffCtl = kOffStage + 4 * 2 * kStageBytes;
     static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
 };
 
 template <int NK, int NV>
 struct alignas(8) WideCtl {
     uint64_t q_full;
+    uint64_t q_empty;    // the S products of a unit are done: Q may be reloaded
     uint64_t k_full[NK];
     uint64_t k_empty[NK];
     uint64_t v_full[NV];
     uint64_t v_empty[NV];
     uint64_t s_full[2];  // per score buffer: S(j) is in TMEM
     uint64_t p_full[2];  // per score buffer: P(j) is in TMEM (and U rescaled)
-    uint64_t o_ready[2];  // by the parity of j: U has absorbed P(j) V_j
+    uint64_t o_ready[2];  // by the parity of g: U has absorbed P(g) V_g
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort;
@@ -98,45 +112,53 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- which rows (one 128-row tile per CTA; longest causal tiles first)
-    const int split = SPLIT ? static_cast<int>(blockIdx.x % p.num_splits) : 0;
-    const int blk = SPLIT ? static_cast<int>(blockIdx.x / p.num_splits) : static_cast<int>(blockIdx.x);
-    const int bh = blk / p.num_q_blocks;
-    int qb = blk % p.num_q_blocks;
-    if (CAUSAL) qb = p.num_q_blocks - 1 - qb;
-    const int b_idx = bh / p.H, h_idx = bh % p.H;
-    const int first_row = qb * kTileM;
     const int nkv = (p.Nk + BN - 1) / BN;
-    int T = nkv;  // key tiles visible to the tile
-    if (CAUSAL) {
-        const int last = min(first_row + kTileM - 1, p.Nq - 1) + p.mask_offset;
-        T = last < 0 ? 0 : min(last / BN + 1, nkv);
-    }
-    int k0 = 0, n = T;  // this CTA visits key tiles k0 .. k0 + n - 1
-    if constexpr (SPLIT) {
-        const int chunk = (T + p.num_splits - 1) / p.num_splits;
-        k0 = split * chunk;
-        n = max(0, min(k0 + chunk, T) - k0);
-        if (n == 0) {  // empty range: its partials carry no weight
-            const int row = first_row + static_cast<int>(threadIdx.x);
-            if (threadIdx.x < kTileM && row < p.Nq) {
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + row;
-                const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
-                p.lse_part[i] = -INFINITY;
-                p.lse_part[plane + i] = -INFINITY;
-            }
-            return;
+    // ---- work units (as in fa_fwd_kernel): CTA c takes units c, 2G - 1 - c,
+    // 2G + c, ...; with the causal mask the longest query tiles come first
+    struct Unit {
+        int bh, qb, split, k0, n;
+    };
+    const int S = SPLIT ? p.num_splits : 1;
+    auto unit_id = [&](int r) {
+        const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+        return r * G + ((r & 1) ? G - 1 - c : c);
+    };
+    auto unit_of = [&](int u) {
+        Unit w;
+        if (CAUSAL) {
+            const int per_qb = p.BH * S;
+            w.qb = p.num_q_blocks - 1 - u / per_qb;
+            w.bh = (u % per_qb) / S;
+            w.split = u % S;
+        } else {
+            w.bh = u / (p.num_q_blocks * S);
+            w.qb = (u / S) % p.num_q_blocks;
+            w.split = u % S;
         }
-    }
+        int T = nkv;  // key tiles visible to the tile
+        if (CAUSAL) {
+            const int last = min(w.qb * kTileM + kTileM - 1, p.Nq - 1) + p.mask_offset;
+            T = last < 0 ? 0 : min(last / BN + 1, nkv);
+        }
+        w.k0 = 0;
+        w.n = T;  // the unit visits key tiles k0 .. k0 + n - 1
+        if constexpr (SPLIT) {
+            const int chunk = (T + S - 1) / S;
+            w.k0 = w.split * chunk;
+            w.n = max(0, min(w.k0 + chunk, T) - w.k0);
+        }
+        return w;
+    };
 
     const uint32_t bar_q = ptx::smem_addr(&ctl->q_full);
+    const uint32_t bar_qe = ptx::smem_addr(&ctl->q_empty);
     auto bar_kf = [&](int s) { return ptx::smem_addr(&ctl->k_full[s]); };
     auto bar_ke = [&](int s) { return ptx::smem_addr(&ctl->k_empty[s]); };
     auto bar_vf = [&](int s) { return ptx::smem_addr(&ctl->v_full[s]); };
     auto bar_ve = [&](int s) { return ptx::smem_addr(&ctl->v_empty[s]); };
     auto bar_sf = [&](int b) { return ptx::smem_addr(&ctl->s_full[b]); };
     auto bar_pf = [&](int b) { return ptx::smem_addr(&ctl->p_full[b]); };
-    auto bar_o = [&](int j) { return ptx::smem_addr(&ctl->o_ready[j & 1]); };
+    auto bar_o = [&](uint32_t g) { return ptx::smem_addr(&ctl->o_ready[g & 1]); };
     const uint32_t bar_drain = ptx::smem_addr(&ctl->drain);
     const uint32_t sQ = sbase + C::kOffQ;
     auto sK = [&](int s) { return sbase + C::kOffK + s * C::kKVBytes; };
@@ -144,6 +166,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_q, 1);
+        ptx::mbar_init(bar_qe, 1);
         for (int s = 0; s < NK; ++s) {
             ptx::mbar_init(bar_kf(s), 1);
             ptx::mbar_init(bar_ke(s), 1);
@@ -179,49 +202,64 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
     if (warp == kWideLoaderWarp) {
         // =============================================================== loader
-        // Q once; then K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V.
+        // Per unit: Q once the previous unit's S products are done, then
+        // K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V.  The
+        // rings run on across units.
         int issued_k[NK], issued_v[NV];
 #pragma unroll
         for (int s = 0; s < NK; ++s) issued_k[s] = 0;
 #pragma unroll
         for (int s = 0; s < NV; ++s) issued_v[s] = 0;
-        if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar_q, C::kQBytes);
+        uint32_t kc = 0, vc = 0;  // K and V tiles loaded so far
+        int nq = 0;               // units whose Q was loaded
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            if (w.n == 0) continue;
+            const int b_idx = w.bh / p.H, h_idx = w.bh % p.H;
+            if (nq > 0 && !(ok = wait_warp(bar_qe, (nq - 1) & 1, abort, tmo))) break;
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar_q, C::kQBytes);
 #pragma unroll
-            for (int c = 0; c < C::kSub; ++c)
-                ptx::tma_load_4d(sQ + c * C::kQSubBytes, &tm_q, bar_q, 64 * c, first_row, h_idx,
-                                 b_idx);
-        }
-        for (int j = 0; j <= n; ++j) {
-            if (j < n) {
-                const int s = j % NK;
-                if (j >= NK && !wait_warp(bar_ke(s), ((j / NK) - 1) & 1, abort, tmo)) break;
-                const bool skip = (p.fault_mode == 1 && j == 0);
-                if (lane == 0 && !skip) {
-                    ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
-#pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
-                                         (k0 + j) * BN, h_idx, b_idx);
-                }
-                if (!skip) ++issued_k[s];
+                for (int c = 0; c < C::kSub; ++c)
+                    ptx::tma_load_4d(sQ + c * C::kQSubBytes, &tm_q, bar_q, 64 * c, w.qb * kTileM, h_idx,
+                                     b_idx);
             }
-            if (j >= 1) {
-                const int jv = j - 1;
-                const int s = jv % NV;
-                if (jv >= NV && !wait_warp(bar_ve(s), ((jv / NV) - 1) & 1, abort, tmo)) break;
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
+            ++nq;
+            for (int j = 0; j <= w.n; ++j) {
+                if (j < w.n) {
+                    const int s = kc % NK;
+                    if (kc >= NK && !(ok = wait_warp(bar_ke(s), ((kc / NK) - 1) & 1, abort, tmo))) break;
+                    const bool skip = (p.fault_mode == 1 && kc == 0);
+                    if (lane == 0 && !skip) {
+                        ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                         (k0 + jv) * BN, h_idx, b_idx);
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
+                                             (w.k0 + j) * BN, h_idx, b_idx);
+                    }
+                    if (!skip) ++issued_k[s];
+                    ++kc;
                 }
-                ++issued_v[s];
+                if (j >= 1) {
+                    const int s = vc % NV;
+                    if (vc >= NV && !(ok = wait_warp(bar_ve(s), ((vc / NV) - 1) & 1, abort, tmo))) break;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
+#pragma unroll
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
+                                             (w.k0 + j - 1) * BN, h_idx, b_idx);
+                    }
+                    ++issued_v[s];
+                    ++vc;
+                }
             }
         }
         // Never leave the CTA with copies still landing in its shared memory.
-        wait_warp(bar_q, 0, abort, tmo, false);
+        if (nq > 0) wait_warp(bar_q, (nq - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NK; ++s)
             if (issued_k[s] > 0) wait_warp(bar_kf(s), (issued_k[s] - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NV; ++s)
@@ -261,34 +299,47 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             __syncwarp();
         };
-        bool ok = n > 0 && wait_warp(bar_q, 0, abort, tmo);
-        for (int j = 0; ok && j < 2 && j < n; ++j) {
-            if (!(ok = wait_warp(bar_kf(j % NK), (j / NK) & 1, abort, tmo))) break;
+        // S of the key tile counted g over all units, from K slot kc % NK;
+        // the last S of a unit also releases its Q
+        uint32_t kc = 0, vc = 0;  // K and V tiles consumed so far (same order as loaded)
+        uint32_t g = 0;           // key tiles of all previous units
+        uint32_t nq = 0;          // units so far (q_full phase)
+        bool ok = true;
+        auto s_tile = [&](uint32_t gg, bool last) {
+            const int s = kc % NK;
+            if (!wait_warp(bar_kf(s), (kc / NK) & 1, abort, tmo)) return false;
             ptx::tc_fence_after_sync();
-            issue_s(j, j % NK);
-            ptx::tc_commit_elect(bar_sf(j));
-            ptx::tc_commit_elect(bar_ke(j % NK));
+            issue_s(gg & 1, s);  // into the buffer PV(gg - 2) has read (issued in order)
+            ptx::tc_commit_elect(bar_sf(gg & 1));
+            ptx::tc_commit_elect(bar_ke(s));
+            if (last) ptx::tc_commit_elect(bar_qe);
+            ++kc;
             __syncwarp();
-        }
-        for (int j = 0; ok && j < n; ++j) {
-            const int b = j & 1;
-            const int sv = j % NV;
-            if (!(ok = wait_warp(bar_vf(sv), (j / NV) & 1, abort, tmo))) break;
-            if (!(ok = wait_warp(bar_pf(b), (j >> 1) & 1, abort, tmo))) break;
-            ptx::tc_fence_after_sync();
-            issue_pv(b, sv, j > 0);
-            ptx::tc_commit_elect(bar_o(j));
-            ptx::tc_commit_elect(bar_ve(sv));
-            __syncwarp();
-            if (j + 2 < n) {
-                const int sk = (j + 2) % NK;
-                if (!(ok = wait_warp(bar_kf(sk), ((j + 2) / NK) & 1, abort, tmo))) break;
+            return true;
+        };
+        for (int r = 0; ok; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            if (w.n == 0) continue;
+            if (!(ok = wait_warp(bar_q, nq & 1, abort, tmo))) break;
+            ++nq;
+            for (int j = 0; ok && j < 2 && j < w.n; ++j) ok = s_tile(g + j, j == w.n - 1);
+            for (int j = 0; ok && j < w.n; ++j) {
+                const uint32_t gg = g + j;
+                const int b = gg & 1;
+                const int sv = vc % NV;
+                if (!(ok = wait_warp(bar_vf(sv), (vc / NV) & 1, abort, tmo))) break;
+                if (!(ok = wait_warp(bar_pf(b), (gg >> 1) & 1, abort, tmo))) break;
                 ptx::tc_fence_after_sync();
-                issue_s(b, sk);  // into the buffer PV(j) has just read (issued in order)
-                ptx::tc_commit_elect(bar_sf(b));
-                ptx::tc_commit_elect(bar_ke(sk));
+                issue_pv(b, sv, j > 0);  // the first product of a unit overwrites U
+                ptx::tc_commit_elect(bar_o(gg));
+                ptx::tc_commit_elect(bar_ve(sv));
+                ++vc;
                 __syncwarp();
+                if (j + 2 < w.n) ok = s_tile(gg + 2, j + 3 == w.n);
             }
+            g += w.n;
         }
         // Drain: nothing of ours may still run on the tensor core at teardown.
         ptx::tc_commit_elect(bar_drain);
@@ -297,7 +348,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     } else {
         // ======================================== softmax + epilogue (warps 0-3)
         const int t = threadIdx.x;                    // row in the tile = TMEM lane
-        const int row = first_row + t;                // query index in the head
+        // of the current unit: the tile's first query index, this thread's,
+        // and the first key tile visited
+        int first_row = 0, row = 0, k0 = 0;
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t u_addr = tmem + lane_off + kWideTmemU;
         const float c2 = p.scale_log2;
@@ -338,117 +391,135 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 add_packed<BF16>(rh[c & 1], pk[c]);
             }
         };
-        float m_ref = -INFINITY;
-        float2 lsum = make_float2(0.f, 0.f);
-        float2 lhat = make_float2(0.f, 0.f);
+        uint32_t g = 0;  // key tiles of all previous units (buffers and barrier phases)
         bool aborted = false;
+        for (int r = 0; !aborted; ++r) {
+            const int u = unit_id(r);
+            if (u >= p.num_units) break;
+            const Unit w = unit_of(u);
+            const int b_idx = w.bh / p.H, h_idx = w.bh % p.H;
+            first_row = w.qb * kTileM;
+            row = first_row + t;
+            k0 = w.k0;
+            const int n = w.n;
+            if (SPLIT && n == 0) {  // empty key range: its partials carry no weight
+                if (row < p.Nq) {
+                    const size_t i = (static_cast<size_t>(w.split) * p.BH + w.bh) * p.Nq + row;
+                    const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
+                    p.lse_part[i] = -INFINITY;
+                    p.lse_part[plane + i] = -INFINITY;
+                }
+                continue;
+            }
+            float m_ref = -INFINITY;
+            float2 lsum = make_float2(0.f, 0.f);
+            float2 lhat = make_float2(0.f, 0.f);
 
-        for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
-            if (!wait_warp(bar_sf(b), (j >> 1) & 1, abort, tmo)) {
-                aborted = true;
-                break;
-            }
-            ptx::tc_fence_after_sync();
-            const uint32_t s_addr = tmem + lane_off + b * BN;
-            uint32_t pk[BN / 2];
-            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            // (tcgen05.ld is warp-collective: every branch around it is uniform)
-            bool redo = (m_ref == -INFINITY);
-            if (!__any_sync(0xffffffffu, redo)) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t sv[32];
-                    load_chunk(s_addr, sv, c, j);
-                    weights(sv, 16, -m_ref * c2, &pk[16 * c], rs, rh);
-                }
-                redo = rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
-            }
-            float alpha = 1.f;
-            float m_new = m_ref;
-            if (__any_sync(0xffffffffu, redo)) {
-                float mt = -INFINITY;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t sv[32];
-                    load_chunk(s_addr, sv, c, j);
-                    float mx[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
-#pragma unroll
-                    for (int u = 4; u + 8 <= 32; u += 8)
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
-                                               __uint_as_float(sv[u + 4 + w]));
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
-                    mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                }
-                if (redo) {
-                    m_new = fmaxf(mt, m_ref);
-                    if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
-                }
-                const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
-                rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t sv[32];
-                    load_chunk(s_addr, sv, c, j);
-                    weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
-                }
-            }
-            const float2 av = make_float2(alpha, alpha);
-            const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
-            lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
-            lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-                ptx::tmem_st_32x32b_x32(s_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
-            // U may still be absorbing P(j-1) V (issued after S(j)): a rescale
-            // waits for that product first (warp-uniform)
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                if (j > 0 && !wait_warp(bar_o(j - 1), ((j - 1) >> 1) & 1, abort, tmo)) {
+            for (int j = 0; j < n; ++j) {
+                const uint32_t gg = g + j;
+                const int b = gg & 1;
+                if (!wait_warp(bar_sf(b), (gg >> 1) & 1, abort, tmo)) {
                     aborted = true;
                     break;
                 }
                 ptx::tc_fence_after_sync();
-#pragma unroll 1
-                for (int c = 0; c < D / 16; ++c) {
-                    uint32_t ov[16];
-                    ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
-                    ptx::tmem_wait_ld();
+                const uint32_t s_addr = tmem + lane_off + b * BN;
+                uint32_t pk[BN / 2];
+                float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float2 rh[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                // (tcgen05.ld is warp-collective: every branch around it is uniform)
+                bool redo = (m_ref == -INFINITY);
+                if (!__any_sync(0xffffffffu, redo)) {
 #pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
-                        ptx::reg_fence(ov[u]);
-                        ptx::reg_fence(ov[u + 1]);
-                        const float2 rr = __fmul2_rn(
-                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), av);
-                        ov[u] = __float_as_uint(rr.x);
-                        ov[u + 1] = __float_as_uint(rr.y);
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t sv[32];
+                        load_chunk(s_addr, sv, c, j);
+                        weights(sv, 16, -m_ref * c2, &pk[16 * c], rs, rh);
                     }
-                    ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
+                    redo = rs[0].x + rs[0].y + rs[1].x + rs[1].y > weight_sum_limit<BF16>();
                 }
+                float alpha = 1.f;
+                float m_new = m_ref;
+                if (__any_sync(0xffffffffu, redo)) {
+                    float mt = -INFINITY;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t sv[32];
+                        load_chunk(s_addr, sv, c, j);
+                        float mx[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) mx[u] = __uint_as_float(sv[u]);
+#pragma unroll
+                        for (int u = 4; u + 8 <= 32; u += 8)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                mx[w] = ptx::fmax3(mx[w], __uint_as_float(sv[u + w]),
+                                                   __uint_as_float(sv[u + 4 + w]));
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) mx[w] = fmaxf(mx[w], __uint_as_float(sv[28 + w]));
+                        mt = ptx::fmax3(mt, fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    }
+                    if (redo) {
+                        m_new = fmaxf(mt, m_ref);
+                        if (m_ref != -INFINITY) alpha = ptx::ex2_approx((m_ref - m_new) * c2);
+                    }
+                    const float neg_ref = (m_new == -INFINITY) ? 0.f : -m_new * c2;
+                    rs[0] = rs[1] = rh[0] = rh[1] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t sv[32];
+                        load_chunk(s_addr, sv, c, j);
+                        weights(sv, 16, neg_ref, &pk[16 * c], rs, rh);
+                    }
+                }
+                const float2 av = make_float2(alpha, alpha);
+                const float2 r = __fadd2_rn(rs[0], rs[1]), hh = __fadd2_rn(rh[0], rh[1]);
+                lsum.x = fmaf(lsum.x, alpha, r.x + r.y);
+                lhat.x = fmaf(lhat.x, alpha, hh.x + hh.y);
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                    ptx::tmem_st_32x32b_x32(s_addr + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+                // U may still be absorbing P(j-1) V (issued after S(j)): a rescale
+                // waits for that product first (warp-uniform)
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    if (j > 0 && !wait_warp(bar_o(gg - 1), ((gg - 1) >> 1) & 1, abort, tmo)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t ov[16];
+                        ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int u = 0; u < 16; u += 2) {
+                            ptx::reg_fence(ov[u]);
+                            ptx::reg_fence(ov[u + 1]);
+                            const float2 rr = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), av);
+                            ov[u] = __float_as_uint(rr.x);
+                            ov[u + 1] = __float_as_uint(rr.y);
+                        }
+                        ptx::tmem_st_32x32b_x16(u_addr + c * 16, ov);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(bar_pf(b));
+                m_ref = m_new;
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar_pf(b));
-            m_ref = m_new;
-        }
 
-        // ---- epilogue: O = U / lhat -> 16-bit -> swizzled smem -> TMA store
-        if (!aborted && n > 0) aborted = !wait_warp(bar_o(n - 1), ((n - 1) >> 1) & 1, abort, tmo);
-        // a tile that sees no key stages its zeros over the Q tile: wait until
-        // the copy of Q has landed, or it could overwrite them
-        if (!SPLIT && !aborted && n == 0) aborted = !wait_warp(bar_q, 0, abort, tmo);
-        const float l_all = lsum.x + lsum.y;
-        const float lhat_all = lhat.x + lhat.y;
-        if constexpr (SPLIT) {
-            if (!aborted) {
+            // ---- epilogue: O = U / lhat -> 16-bit -> per-warp staging boxes -> TMA
+            if (!aborted && n > 0) aborted = !wait_warp(bar_o(g + n - 1), ((g + n - 1) >> 1) & 1, abort, tmo);
+            g += n;
+            if (aborted) break;
+            const float l_all = lsum.x + lsum.y;
+            const float lhat_all = lhat.x + lhat.y;
+            if constexpr (SPLIT) {
                 const bool mine = row < p.Nq && !*abort;
                 const bool any = l_all > 0.f;
-                const size_t i = (static_cast<size_t>(split) * p.BH + bh) * p.Nq + (mine ? row : 0);
+                const size_t i = (static_cast<size_t>(w.split) * p.BH + w.bh) * p.Nq + (mine ? row : 0);
                 const size_t plane = static_cast<size_t>(p.num_splits) * p.BH * p.Nq;
                 if (mine) {
                     p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
@@ -463,68 +534,74 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; u += 4) {
-                        ptx::reg_fence(ov[u]);
-                        ptx::reg_fence(ov[u + 1]);
-                        ptx::reg_fence(ov[u + 2]);
-                        ptx::reg_fence(ov[u + 3]);
+                    for (int e = 0; e < 32; e += 4) {
+                        ptx::reg_fence(ov[e]);
+                        ptx::reg_fence(ov[e + 1]);
+                        ptx::reg_fence(ov[e + 2]);
+                        ptx::reg_fence(ov[e + 3]);
                         if (mine)
-                            dst[c * 8 + u / 4] = make_float4(
-                                __uint_as_float(ov[u]) * inv, __uint_as_float(ov[u + 1]) * inv,
-                                __uint_as_float(ov[u + 2]) * inv, __uint_as_float(ov[u + 3]) * inv);
+                            dst[c * 8 + e / 4] = make_float4(
+                                __uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
+                                __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
                     }
                 }
-            }
-        } else if (!aborted) {
-            ptx::tc_fence_after_sync();
-            const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
-            const float2 iv = make_float2(inv, inv);
+            } else {
+                // each warp stores its 32 rows, 64 columns at a time, through two
+                // staging boxes used in turn (128-byte swizzle, as the TMA store
+                // expects); rows >= Nq and columns >= d are clipped
+                ptx::tc_fence_after_sync();
+                const bool mine = row < p.Nq && !*abort;
+                const float inv = lhat_all > 0.f ? 1.f / lhat_all : 0.f;
+                const float2 iv = make_float2(inv, inv);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                if (n > 0) {
-                    ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
-                    ptx::tmem_wait_ld();
+                for (int h = 0; h < C::kSub; ++h) {
+                    const uint32_t stage = sbase + C::kOffStage + (warp * 2 + (h & 1)) * C::kStageBytes;
+                    // the store that last used this box (two stores back) has read it
+                    if (lane == 0) ptx::bulk_wait_group_read1();
+                    __syncwarp();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) ptx::reg_fence(ov[u]);
-                } else {  // no key visible to this tile: O = 0 (U was never written)
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t ov[32];
+                        if (n > 0) {
+                            ptx::tmem_ld_32x32b_x32(u_addr + (2 * h + cc) * 32, ov);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) ov[u] = 0u;
-                }
-                // the Q tile is free now (every S product is done) and becomes
-                // the staging buffer, 128-byte swizzled as the TMA store expects
-                const uint32_t sub = sQ + (c >> 1) * C::kQSubBytes + t * 128;
+                            for (int e = 0; e < 32; ++e) ptx::reg_fence(ov[e]);
+                        } else {  // no key visible to this tile: O = 0 (U was not written)
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = (c & 1) * 4 + q4;
-                    uint32_t w[4];
+                            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+                        }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int u = q4 * 8 + 2 * e;
-                        const float2 o2 = __fmul2_rn(
-                            make_float2(__uint_as_float(ov[u]), __uint_as_float(ov[u + 1])), iv);
-                        w[e] = pack2<BF16>(o2.x, o2.y);
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t wv[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c8 = q4 * 8 + 2 * e;
+                                const float2 o2 = __fmul2_rn(
+                                    make_float2(__uint_as_float(ov[c8]), __uint_as_float(ov[c8 + 1])), iv);
+                                wv[e] = pack2<BF16>(o2.x, o2.y);
+                            }
+                            const uint32_t dst = stage + lane * 128 + (((cc * 4 + q4) ^ (lane & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(wv[0]),
+                                         "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                                         : "memory");
+                        }
                     }
-                    const uint32_t dst = sub + ((chunk ^ (t & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]),
-                                 "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                 : "memory");
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && !*abort) {
+                        ptx::tma_store_4d(&tm_o, stage, 64 * h, first_row + 32 * warp, h_idx, b_idx);
+                        ptx::bulk_commit_group();
+                    }
+                }
+                if (mine) {
+                    const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
+                    p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
                 }
             }
-            ptx::fence_proxy_async_smem();
-        }
-        ptx::named_barrier_sync(1, kTileM);
-        if (!SPLIT && t == 0 && !*abort) {
-#pragma unroll
-            for (int c = 0; c < C::kSub; ++c)
-                ptx::tma_store_4d(&tm_o, sQ + c * C::kQSubBytes, 64 * c, first_row, h_idx, b_idx);
-            ptx::bulk_commit_group();
-            ptx::bulk_wait_group_read0();
-        }
-        if (!SPLIT && !aborted && !*abort && row < p.Nq) {
-            const float lse = (l_all > 0.f) ? m_ref * p.scale + logf(l_all) : -INFINITY;
-            p.lse[b_idx * p.lse_sb + h_idx * p.lse_sh + row] = lse;
-        }
+        }  // units
+        // the CTA's shared memory must outlive the stores that read it
+        if (lane == 0) ptx::bulk_wait_group0();
     }
 
     // ---- teardown: every tcgen05 op of this CTA has completed

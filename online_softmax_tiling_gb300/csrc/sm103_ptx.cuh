@@ -128,6 +128,12 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most one of this thread's bulk store groups is still
+// reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Wait until this thread's bulk stores have fully completed (not only read
 // their shared-memory source).
 __device__ __forceinline__ void bulk_wait_group0() {

@@ -36,13 +36,16 @@ CASES = [  # (B, H, Nq, Nk, d, dtype, mask, splits)
     (2, 100, 600, 600, 128, synth.FP16, 1, 1),    # 600 causal units, longest first
     (2, 60, 900, 900, 64, synth.BF16, 1, 3),      # 1440 units: causal, three key ranges each
     (1, 200, 256, 256, 128, synth.BF16, 0, 1),    # 200 units of two key tiles
+    (2, 40, 700, 300, 256, synth.BF16, 2, 1),     # wide heads: 480 units, some see no key
+    (1, 60, 500, 500, 192, synth.FP16, 1, 2),     # wide heads: 480 causal units, two key ranges
 ]
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d,dtype,mask,splits", CASES)
 def test_many_units_per_cta(B, H, Nq, Nk, d, dtype, mask, splits):
     import online_softmax_tiling_gb300 as fa
-    units = B * H * ((Nq + 255) // 256) * splits
+    block = 256 if d <= 128 else 128  # query rows per unit
+    units = B * H * ((Nq + block - 1) // block) * splits
     assert units > _sms(), "the shape must give some CTA more than one unit"
     seed = 710000 + 11 * H + Nq + 3 * Nk + d + 5 * mask + splits
     q = synth.tensor_bits(seed, (B, H, Nq, d), dtype)
