@@ -13,8 +13,9 @@
  *   side output s*m + ln(l) of section "最后：归一化并写回 O".
  *
  * The library computes this in one kernel launch, FlashAttention-2 loop
- * order (one CTA per 128-row query tile, key/value tiles streamed through
- * shared memory, scores and weights kept in tensor memory, never in HBM).
+ * order (query tiles of 128 rows, walked by one persistent CTA per SM;
+ * key/value tiles streamed through shared memory; scores and weights kept
+ * in tensor memory, never in HBM).
  *
  * This header needs no CUDA header: streams are passed as void*.
  */

@@ -82,7 +82,7 @@ struct KernelEntry {
     const void* fn;
     int smem;
     int threads;
-    int block_m;  // query rows per CTA
+    int block_m;  // query rows per unit of work
     int block_n;  // keys per K/V tile (rows of the K and V boxes)
 };
 
@@ -169,9 +169,9 @@ int choose_splits(int64_t BH, int Nq, int Nk, int kd) {
     if (kd == 0) return 1;
     const int sms = sm_count();
     const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
-    const int64_t ctas = BH * ((Nq + block_m - 1) / block_m);
-    if (2 * ctas > sms) return 1;
-    int64_t s = (static_cast<int64_t>(sms) + ctas - 1) / ctas;
+    const int64_t blocks = BH * ((Nq + block_m - 1) / block_m);
+    if (2 * blocks > sms) return 1;
+    int64_t s = (static_cast<int64_t>(sms) + blocks - 1) / blocks;
     s = std::min<int64_t>(s, std::max<int64_t>(1, static_cast<int64_t>(Nk) / 512));
     s = std::min<int64_t>(s, FA_MAX_SPLITS);
     return static_cast<int>(std::max<int64_t>(1, s));
@@ -213,7 +213,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     const bool causal = a.mask != FA_MASK_NONE;
     const int64_t BH = static_cast<int64_t>(B) * H;
     const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
-    const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // CTAs per head
+    const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // query blocks per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
     // TMA: every stride a positive multiple of 16 bytes (8 16-bit elements);
     // LSE rows contiguous, its strides positive

@@ -9,13 +9,18 @@
 //
 // How it maps onto the GB300 SM (the pages' SM80 cp.async / mma.sync design is
 // prior art only):
-//   * one CTA per pair of 128-row query tiles (A, B) of one (batch, head);
-//     both tiles share every K/V tile that lands in shared memory.  10 warps:
+//   * a persistent grid (one CTA per SM) walks units: a unit is a pair of
+//     128-row query tiles (A, B) of one (batch, head), and with split-KV one
+//     key range of it; both tiles share every K/V tile that lands in shared
+//     memory.  Rings, barrier phases and TMEM run on from one unit to the
+//     next, so the next unit's Q and first products overlap this unit's
+//     last tiles and epilogue.  10 warps:
 //       warps 0-3  softmax + epilogue of tile A, warps 4-7 the same for B:
 //                  thread t owns query row t of its tile (= TMEM lane t), so
 //                  the row max and row sums need no shuffles;
-//       warp 8     loader: TMA (cp.async.bulk.tensor) of both Q tiles once,
-//                  then K tiles running ahead of V tiles through two rings;
+//       warp 8     loader: TMA (cp.async.bulk.tensor) of both Q tiles of a
+//                  unit, then K tiles running ahead of V tiles through two
+//                  rings;
 //       warp 9     tensor-core issuer: warp-uniform loop, elect.sync lane
 //                  issues tcgen05.mma.
 //   * TMEM (512 columns): S_A at 0, S_B at 128 (128 fp32 columns each; the
@@ -46,7 +51,8 @@
 //     of the fp32 weights.
 //   * key tiles wholly in the future are skipped and the diagonal tile is
 //     masked element-wise ("causal 模式在哪一步生效"); keys >= N (zero-filled by
-//     TMA) are masked; query rows >= N are clipped by the TMA store.
+//     TMA) are masked; query rows >= N are clipped by the TMA store, which
+//     each softmax warp issues for its 32 rows from its own staging box.
 //   * every mbarrier wait is bounded; on expiry the CTA records FA_ERR_TIMEOUT
 //     in a device status word, drains its in-flight copies and MMAs, frees
 //     its TMEM and exits.
@@ -61,7 +67,7 @@
 namespace fa {
 
 constexpr int kTileM = 128;           // rows per query tile (= TMEM lanes = MMA M)
-constexpr int kBlockM = 2 * kTileM;   // rows per CTA (tiles A and B)
+constexpr int kBlockM = 2 * kTileM;   // rows per unit of work (tiles A and B)
 constexpr int kBlockN = 128;          // keys per tile (= MMA N of S = Q K^T)
 constexpr int kThreads = 320;         // 8 softmax warps + loader warp + MMA warp
 constexpr int kLoaderWarp = 8;
