@@ -63,8 +63,10 @@ struct WideCfg {
     static constexpr int kKVSubBytes = kWideBlockN * 128;    // 128 rows x 128 bytes
     static constexpr int kQBytes = kSub * kQSubBytes;
     static constexpr int kKVBytes = kSub * kKVSubBytes;
-    static constexpr int kKStages = D == 256 ? 1 : 2;
-    static constexpr int kVStages = 1;
+    // one K and one V slot for d = 256; for d = 192 the second slot goes to V,
+    // whose slot frees only when P.V is done (K's when the shorter S is)
+    static constexpr int kKStages = 1;
+    static constexpr int kVStages = D == 256 ? 1 : 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
@@ -228,33 +230,44 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                                      b_idx);
             }
             ++nq;
-            for (int j = 0; j <= w.n; ++j) {
-                if (j < w.n) {
-                    const int s = kc % NK;
-                    if (kc >= NK && !(ok = wait_warp(bar_ke(s), ((kc / NK) - 1) & 1, abort, tmo))) break;
-                    const bool skip = (p.fault_mode == 1 && kc == 0);
-                    if (lane == 0 && !skip) {
-                        ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
+            // K tile j and V tile j - 1; with more V slots than K slots the V
+            // tile goes first, since the K slot frees only when S(j - 1) is done
+            auto load_k = [&](int j) {
+                const int s = kc % NK;
+                if (kc >= NK && !wait_warp(bar_ke(s), ((kc / NK) - 1) & 1, abort, tmo)) return false;
+                const bool skip = (p.fault_mode == 1 && kc == 0);
+                if (lane == 0 && !skip) {
+                    ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
 #pragma unroll
-                        for (int c = 0; c < C::kSub; ++c)
-                            ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
-                                             (w.k0 + j) * BN, h_idx, b_idx);
-                    }
-                    if (!skip) ++issued_k[s];
-                    ++kc;
+                    for (int c = 0; c < C::kSub; ++c)
+                        ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
+                                         (w.k0 + j) * BN, h_idx, b_idx);
                 }
-                if (j >= 1) {
-                    const int s = vc % NV;
-                    if (vc >= NV && !(ok = wait_warp(bar_ve(s), ((vc / NV) - 1) & 1, abort, tmo))) break;
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
+                if (!skip) ++issued_k[s];
+                ++kc;
+                return true;
+            };
+            auto load_v = [&](int j) {
+                const int s = vc % NV;
+                if (vc >= NV && !wait_warp(bar_ve(s), ((vc / NV) - 1) & 1, abort, tmo)) return false;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
 #pragma unroll
-                        for (int c = 0; c < C::kSub; ++c)
-                            ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                             (w.k0 + j - 1) * BN, h_idx, b_idx);
-                    }
-                    ++issued_v[s];
-                    ++vc;
+                    for (int c = 0; c < C::kSub; ++c)
+                        ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
+                                         (w.k0 + j) * BN, h_idx, b_idx);
+                }
+                ++issued_v[s];
+                ++vc;
+                return true;
+            };
+            for (int j = 0; j <= w.n; ++j) {
+                if constexpr (NV > NK) {
+                    if (j >= 1 && !(ok = load_v(j - 1))) break;
+                    if (j < w.n && !(ok = load_k(j))) break;
+                } else {
+                    if (j < w.n && !(ok = load_k(j))) break;
+                    if (j >= 1 && !(ok = load_v(j - 1))) break;
                 }
             }
         }
