@@ -83,7 +83,8 @@ struct KernelEntry {
     int smem;
     int threads;
     int block_m;  // query rows per unit of work
-    int block_n;  // keys per K/V tile (rows of the K and V boxes)
+    int block_n;  // keys per K/V tile (rows of the K boxes)
+    int v_rows;   // rows of the V boxes (a tile or a part of one)
 };
 
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
@@ -91,11 +92,12 @@ KernelEntry entry() {
     if constexpr (D <= 128)
         return KernelEntry{
             reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>),
-            fa::Cfg<D>::kSmemBytes, fa::kThreads, fa::kBlockM, fa::kBlockN};
+            fa::Cfg<D>::kSmemBytes, fa::kThreads, fa::kBlockM, fa::kBlockN, fa::kBlockN};
     else
         return KernelEntry{
             reinterpret_cast<const void*>(&fa::fa_fwd_wide_kernel<D, BF16, CAUSAL, SPLIT>),
-            fa::WideCfg<D>::kSmemBytes, fa::kWideThreads, fa::kTileM, fa::kWideBlockN};
+            fa::WideCfg<D>::kSmemBytes, fa::kWideThreads, fa::kTileM, fa::kWideBlockN,
+            fa::WideCfg<D>::kVPartRows};
 }
 
 template <int D, bool BF16>
@@ -244,7 +246,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     CUtensorMap tq, tk, tv, to;
     if (!encode_4d(&tq, a.q, dtype, B, H, Nq, d, a.q_stride, qrows) ||
         !encode_4d(&tk, a.k, dtype, B, H, Nk, d, a.k_stride, krows) ||
-        !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride, krows) ||
+        !encode_4d(&tv, a.v, dtype, B, H, Nk, d, a.v_stride, static_cast<uint32_t>(ke.v_rows)) ||
         !encode_4d(&to, a.o, dtype, B, H, Nq, d, a.o_stride, 32u))  // one warp's rows per store
         return FA_ERR_CUDA;
 

@@ -67,6 +67,11 @@ struct WideCfg {
     // whose slot frees only when P.V is done (K's when the shorter S is)
     static constexpr int kKStages = 1;
     static constexpr int kVStages = D == 256 ? 1 : 2;
+    // With one V slot (d = 256) each V tile travels as two 64-key parts with
+    // their own barriers: P.V runs part by part, and the next tile's first
+    // part loads while this tile's second part is in use.
+    static constexpr int kVParts = D == 256 ? 2 : 1;
+    static constexpr int kVPartRows = kWideBlockN / kVParts;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kQBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
@@ -77,7 +82,7 @@ struct WideCfg {
     static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
 };
 
-template <int NK, int NV>
+template <int NK, int NV>  // NV: V barrier pairs (slots x parts)
 struct alignas(8) WideCtl {
     uint64_t q_full;
     uint64_t q_empty;    // the S products of a unit are done: Q may be reloaded
@@ -107,7 +112,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = ptx::smem_addr(smem);
-    WideCtl<NK, NV>* ctl = reinterpret_cast<WideCtl<NK, NV>*>(smem + C::kOffCtl);
+    constexpr int VP = C::kVParts;
+    WideCtl<NK, NV * VP>* ctl = reinterpret_cast<WideCtl<NK, NV * VP>*>(smem + C::kOffCtl);
     volatile uint32_t* abort = &ctl->abort;
     const unsigned long long tmo = p.timeout_ns;
 
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             ptx::mbar_init(bar_kf(s), 1);
             ptx::mbar_init(bar_ke(s), 1);
         }
-        for (int s = 0; s < NV; ++s) {
+        for (int s = 0; s < NV * VP; ++s) {
             ptx::mbar_init(bar_vf(s), 1);
             ptx::mbar_init(bar_ve(s), 1);
         }
@@ -207,11 +213,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // Per unit: Q once the previous unit's S products are done, then
         // K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V.  The
         // rings run on across units.
-        int issued_k[NK], issued_v[NV];
+        int issued_k[NK], issued_v[NV * VP];
 #pragma unroll
         for (int s = 0; s < NK; ++s) issued_k[s] = 0;
 #pragma unroll
-        for (int s = 0; s < NV; ++s) issued_v[s] = 0;
+        for (int s = 0; s < NV * VP; ++s) issued_v[s] = 0;
         uint32_t kc = 0, vc = 0;  // K and V tiles loaded so far
         int nq = 0;               // units whose Q was loaded
         bool ok = true;
@@ -249,15 +255,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             };
             auto load_v = [&](int j) {
                 const int s = vc % NV;
-                if (vc >= NV && !wait_warp(bar_ve(s), ((vc / NV) - 1) & 1, abort, tmo)) return false;
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar_vf(s), C::kKVBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes, &tm_v, bar_vf(s), 64 * c,
-                                         (w.k0 + j) * BN, h_idx, b_idx);
+                for (int h = 0; h < VP; ++h) {
+                    const int bi = s * VP + h;
+                    if (vc >= NV && !wait_warp(bar_ve(bi), ((vc / NV) - 1) & 1, abort, tmo)) return false;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar_vf(bi), C::kKVBytes / VP);
+#pragma unroll
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sV(s) + c * C::kKVSubBytes + h * C::kVPartRows * 128, &tm_v,
+                                             bar_vf(bi), 64 * c, (w.k0 + j) * BN + h * C::kVPartRows,
+                                             h_idx, b_idx);
+                    }
+                    ++issued_v[bi];
                 }
-                ++issued_v[s];
                 ++vc;
                 return true;
             };
@@ -275,7 +286,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (nq > 0) wait_warp(bar_q, (nq - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NK; ++s)
             if (issued_k[s] > 0) wait_warp(bar_kf(s), (issued_k[s] - 1) & 1, abort, tmo, false);
-        for (int s = 0; s < NV; ++s)
+        for (int s = 0; s < NV * VP; ++s)
             if (issued_v[s] > 0) wait_warp(bar_vf(s), (issued_v[s] - 1) & 1, abort, tmo, false);
     } else if (warp == kWideMmaWarp) {
         // ====================================================== tensor-core issuer
@@ -302,11 +313,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         };
         // U (+)= P_b V_s: 128 keys = 8 steps of K16; P advances 8 TMEM columns
         // (16 packed 16-bit weights), V 16 rows = 2048 bytes per step
-        auto issue_pv = [&](int b, int s, bool acc) {
+        // steps [k_begin, k_end) of U (+)= P_b V_s: 128 keys = 8 steps of K16;
+        // P advances 8 TMEM columns (16 packed 16-bit weights), V 16 rows =
+        // 2048 bytes per step
+        auto issue_pv = [&](int b, int s, bool acc, int k_begin, int k_end) {
             if (ptx::elect_one()) {
                 const uint64_t vd = v_desc0 + s * kStageStep;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
+                for (int k = k_begin; k < k_end; ++k)
                     ptx::mma_ts(tmem + kWideTmemU, tmem + b * BN + k * 8, vd + k * 128, idesc_pv,
                                 (acc || k > 0) ? 1u : 0u);
             }
@@ -342,12 +356,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                 const uint32_t gg = g + j;
                 const int b = gg & 1;
                 const int sv = vc % NV;
-                if (!(ok = wait_warp(bar_vf(sv), (vc / NV) & 1, abort, tmo))) break;
                 if (!(ok = wait_warp(bar_pf(b), (gg >> 1) & 1, abort, tmo))) break;
-                ptx::tc_fence_after_sync();
-                issue_pv(b, sv, j > 0);  // the first product of a unit overwrites U
+                // part by part as V arrives; each part's slot is released
+                // once the product that read it is done
+#pragma unroll
+                for (int h = 0; h < VP; ++h) {
+                    if (!(ok = wait_warp(bar_vf(sv * VP + h), (vc / NV) & 1, abort, tmo))) break;
+                    ptx::tc_fence_after_sync();
+                    // the first product of a unit overwrites U
+                    issue_pv(b, sv, j > 0, h * (BN / 16) / VP, (h + 1) * (BN / 16) / VP);
+                    ptx::tc_commit_elect(bar_ve(sv * VP + h));
+                }
+                if (!ok) break;
                 ptx::tc_commit_elect(bar_o(gg));
-                ptx::tc_commit_elect(bar_ve(sv));
                 ++vc;
                 __syncwarp();
                 if (j + 2 < w.n) ok = s_tile(gg + 2, j + 3 == w.n);
