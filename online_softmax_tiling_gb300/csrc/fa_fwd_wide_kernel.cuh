@@ -82,7 +82,7 @@ struct WideCfg {
     static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
 };
 
-template <int NK, int NV>  // NV: V barrier pairs (slots x parts)
+template <int NK, int NV>  // barrier pairs: NK for K (slots x parts), NV for V
 struct alignas(8) WideCtl {
     uint64_t q_full;
     uint64_t q_empty;    // the S products of a unit are done: Q may be reloaded
@@ -113,7 +113,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = ptx::smem_addr(smem);
     constexpr int VP = C::kVParts;
-    WideCtl<NK, NV * VP>* ctl = reinterpret_cast<WideCtl<NK, NV * VP>*>(smem + C::kOffCtl);
+    // K tiles travel as their 64-column sub-tiles, each with its own barriers:
+    // S = Q K^T reads them in that order (four K16 steps each), so S can start
+    // on the first while the rest land, and each frees as soon as S is past it
+    constexpr int KP = C::kSub;
+    WideCtl<NK * KP, NV * VP>* ctl = reinterpret_cast<WideCtl<NK * KP, NV * VP>*>(smem + C::kOffCtl);
     volatile uint32_t* abort = &ctl->abort;
     const unsigned long long tmo = p.timeout_ns;
 
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_q, 1);
         ptx::mbar_init(bar_qe, 1);
-        for (int s = 0; s < NK; ++s) {
+        for (int s = 0; s < NK * KP; ++s) {
             ptx::mbar_init(bar_kf(s), 1);
             ptx::mbar_init(bar_ke(s), 1);
         }
@@ -213,9 +217,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // Per unit: Q once the previous unit's S products are done, then
         // K_0, K_1, V_0, K_2, V_1, ...: K runs one tile ahead of V.  The
         // rings run on across units.
-        int issued_k[NK], issued_v[NV * VP];
+        int issued_k[NK * KP], issued_v[NV * VP];
 #pragma unroll
-        for (int s = 0; s < NK; ++s) issued_k[s] = 0;
+        for (int s = 0; s < NK * KP; ++s) issued_k[s] = 0;
 #pragma unroll
         for (int s = 0; s < NV * VP; ++s) issued_v[s] = 0;
         uint32_t kc = 0, vc = 0;  // K and V tiles loaded so far
@@ -240,16 +244,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             // tile goes first, since the K slot frees only when S(j - 1) is done
             auto load_k = [&](int j) {
                 const int s = kc % NK;
-                if (kc >= NK && !wait_warp(bar_ke(s), ((kc / NK) - 1) & 1, abort, tmo)) return false;
                 const bool skip = (p.fault_mode == 1 && kc == 0);
-                if (lane == 0 && !skip) {
-                    ptx::mbar_arrive_expect_tx(bar_kf(s), C::kKVBytes);
 #pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(s), 64 * c,
+                for (int c = 0; c < KP; ++c) {
+                    const int bi = s * KP + c;
+                    if (kc >= NK && !wait_warp(bar_ke(bi), ((kc / NK) - 1) & 1, abort, tmo)) return false;
+                    if (lane == 0 && !skip) {
+                        ptx::mbar_arrive_expect_tx(bar_kf(bi), C::kKVSubBytes);
+                        ptx::tma_load_4d(sK(s) + c * C::kKVSubBytes, &tm_k, bar_kf(bi), 64 * c,
                                          (w.k0 + j) * BN, h_idx, b_idx);
+                    }
+                    if (!skip) ++issued_k[bi];
                 }
-                if (!skip) ++issued_k[s];
                 ++kc;
                 return true;
             };
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         }
         // Never leave the CTA with copies still landing in its shared memory.
         if (nq > 0) wait_warp(bar_q, (nq - 1) & 1, abort, tmo, false);
-        for (int s = 0; s < NK; ++s)
+        for (int s = 0; s < NK * KP; ++s)
             if (issued_k[s] > 0) wait_warp(bar_kf(s), (issued_k[s] - 1) & 1, abort, tmo, false);
         for (int s = 0; s < NV * VP; ++s)
             if (issued_v[s] > 0) wait_warp(bar_vf(s), (issued_v[s] - 1) & 1, abort, tmo, false);
@@ -297,13 +303,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // V is MN-major: the next 64 columns of d are one sub-tile further on
         const uint64_t v_desc0 = smem_desc(sV(0), C::kKVSubBytes, 1024);
         constexpr uint64_t kStageStep = C::kKVBytes / 16;
-        // S_b = Q K_s^T: d/16 steps of K16; +32 bytes per step inside a
-        // 128-byte swizzle row, the next 64-column sub-tile after four steps
-        auto issue_s = [&](int b, int s) {
+        // S_b = Q K_s^T over the 64-column sub-tile c of d: four K16 steps,
+        // +32 bytes per step inside a 128-byte swizzle row
+        auto issue_s = [&](int b, int s, int c) {
             if (ptx::elect_one()) {
                 const uint64_t kd = k_desc0 + s * kStageStep;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 4 * c; k < 4 * c + 4; ++k) {
                     const uint64_t ao = (k >> 2) * (C::kQSubBytes / 16) + (k & 3) * 2;
                     const uint64_t bo = (k >> 2) * (C::kKVSubBytes / 16) + (k & 3) * 2;
                     ptx::mma_ss(tmem + b * BN, q_desc + ao, kd + bo, idesc_s, k > 0 ? 1u : 0u);
@@ -334,11 +340,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         bool ok = true;
         auto s_tile = [&](uint32_t gg, bool last) {
             const int s = kc % NK;
-            if (!wait_warp(bar_kf(s), (kc / NK) & 1, abort, tmo)) return false;
-            ptx::tc_fence_after_sync();
-            issue_s(gg & 1, s);  // into the buffer PV(gg - 2) has read (issued in order)
+#pragma unroll
+            for (int c = 0; c < KP; ++c) {
+                if (!wait_warp(bar_kf(s * KP + c), (kc / NK) & 1, abort, tmo)) return false;
+                ptx::tc_fence_after_sync();
+                issue_s(gg & 1, s, c);  // into the buffer PV(gg - 2) has read (issued in order)
+                ptx::tc_commit_elect(bar_ke(s * KP + c));
+            }
             ptx::tc_commit_elect(bar_sf(gg & 1));
-            ptx::tc_commit_elect(bar_ke(s));
             if (last) ptx::tc_commit_elect(bar_qe);
             ++kc;
             __syncwarp();
