@@ -72,26 +72,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled load global -> shared, completion signalled on `bar` (tx bytes).
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// 3-D tiled store shared -> global (out-of-range rows are clipped by the unit).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
-                                             int32_t c1, int32_t c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
-        " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-        "r"(src), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
 // 4-D forms: (column, row, head, batch) coordinates of a strided tensor.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
@@ -100,15 +80,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
-}
-
-// Prefetch a tile of a 4-D tensor into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int32_t c0, int32_t c1,
-                                                int32_t c2, int32_t c3) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int32_t c0,
@@ -174,14 +145,6 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
 // D (tmem) (+)= A (smem descriptor) * B (smem descriptor)^T, kind::f16.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -204,31 +167,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// Warp-uniform forms: every lane executes the instruction with identical
-// operands and elect.sync lets exactly one lane issue it, so descriptor
-// arithmetic stays uniform and the issuing thread never diverges.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // True in exactly one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one() {
     uint32_t r;
@@ -238,6 +176,8 @@ __device__ __forceinline__ bool elect_one() {
     return r != 0u;
 }
 
+// One elected lane arrives once on `bar` when every tcgen05 operation that
+// lane issued so far has completed.
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -300,33 +240,6 @@ __device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a0, uint64_
         "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p1;\n\t}" ::"r"(d_tmem),
         "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// TS form (A = P from tensor memory, B = V MN-major), K = 128 keys: 8 steps.
-__device__ __forceinline__ void mma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p0, %4, 0;\n\t"
-        "setp.eq.b32 p1, %4, %4;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
-        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t"
-        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, p1;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
