@@ -362,6 +362,12 @@ def run_ours(args):
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": traffic, "peak_source": f"{peak_src} bf16_tflops (burst)",
                     "kernel_hash": khash}
+        if "bf16_tflops_sustained" in peaks:
+            # for context only: the same GEMM held for seconds under the power
+            # cap, as long timed regions of this kernel are
+            sus = float(peaks["bf16_tflops_sustained"])
+            roofline["peak_sustained"] = sus
+            roofline["frac_of_sustained"] = round(achieved / sus, 4)
     if traffic is not None:
         # measured DRAM bytes of one launch over this run's time per launch
         roofline["dram_gbps"] = round(traffic / (dev_ms / args.steps * 1e-3) / 1e9, 1)
