@@ -69,6 +69,24 @@ bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The split-KV partials o_part [S][BH][Nq][kd] fp32 viewed by TMA in 4-D
+// (kd, Nq, BH, S): rows >= Nq of a head are clipped on store.  Box: 32
+// columns (128 bytes, one swizzle span) x 32 rows (one softmax warp's rows).
+bool encode_partials(CUtensorMap* map, float* o_part, int64_t S, int64_t BH, int64_t Nq, int64_t kd) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kd), static_cast<cuuint64_t>(Nq),
+                                static_cast<cuuint64_t>(BH), static_cast<cuuint64_t>(S)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kd) * 4,
+                                   static_cast<cuuint64_t>(Nq * kd) * 4,
+                                   static_cast<cuuint64_t>(BH * Nq * kd) * 4};
+    const cuuint32_t box[4] = {32, 32, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, o_part, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Width of the kernel that serves head dimension d: 64, 128, 192 or 256,
 // the smallest that holds d (the columns beyond d are zeros: TMA fills them
 // on load and clips them on store); 0 = unsupported (d must be a multiple of
@@ -276,6 +294,8 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
                                                     split_o_bytes(num_splits, BH, Nq, kd))
                          : nullptr;
 
+    // split-KV kernels write no O: their last tensor map is that of the partials
+    if (split && !encode_partials(&to, prm.o_part, num_splits, BH, Nq, kd)) return FA_ERR_CUDA;
     void* args[] = {&tq, &tk, &tv, &to, &prm};
     // the kernels are persistent: one CTA per SM walks the units
     const int64_t ctas = std::min<int64_t>(units, sm_count());

@@ -317,8 +317,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             __syncwarp();
         };
-        // U (+)= P_b V_s: 128 keys = 8 steps of K16; P advances 8 TMEM columns
-        // (16 packed 16-bit weights), V 16 rows = 2048 bytes per step
         // steps [k_begin, k_end) of U (+)= P_b V_s: 128 keys = 8 steps of K16;
         // P advances 8 TMEM columns (16 packed 16-bit weights), V 16 rows =
         // 2048 bytes per step
@@ -568,24 +566,37 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                     p.lse_part[i] = any ? m_ref * p.scale + logf(l_all) : -INFINITY;
                     p.lse_part[plane + i] = any ? m_ref * p.scale + logf(lhat_all) : -INFINITY;
                 }
+                // O through the warp's two staging boxes in turn, 32 fp32
+                // columns at a time (tm_o maps the partials here; rows >= Nq
+                // clipped)
                 ptx::tc_fence_after_sync();
                 const float inv = any ? 1.f / lhat_all : 0.f;
-                float4* dst = reinterpret_cast<float4*>(p.o_part + i * D);
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
+                    const uint32_t stage = sbase + C::kOffStage + (warp * 2 + (c & 1)) * C::kStageBytes;
                     uint32_t ov[32];
                     ptx::tmem_ld_32x32b_x32(u_addr + c * 32, ov);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        ptx::reg_fence(ov[e]);
-                        ptx::reg_fence(ov[e + 1]);
-                        ptx::reg_fence(ov[e + 2]);
-                        ptx::reg_fence(ov[e + 3]);
-                        if (mine)
-                            dst[c * 8 + e / 4] = make_float4(
-                                __uint_as_float(ov[e]) * inv, __uint_as_float(ov[e + 1]) * inv,
-                                __uint_as_float(ov[e + 2]) * inv, __uint_as_float(ov[e + 3]) * inv);
+                    for (int e = 0; e < 32; ++e) ptx::reg_fence(ov[e]);
+                    // the store that last used this box (two stores back) has read it
+                    if (lane == 0) ptx::bulk_wait_group_read1();
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t dst = stage + lane * 128 + ((q ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                                     "f"(__uint_as_float(ov[4 * q]) * inv),
+                                     "f"(__uint_as_float(ov[4 * q + 1]) * inv),
+                                     "f"(__uint_as_float(ov[4 * q + 2]) * inv),
+                                     "f"(__uint_as_float(ov[4 * q + 3]) * inv)
+                                     : "memory");
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && !*abort) {
+                        ptx::tma_store_4d(&tm_o, stage, 32 * c, first_row + 32 * warp, w.bh, w.split);
+                        ptx::bulk_commit_group();
                     }
                 }
             } else {
