@@ -137,8 +137,10 @@ int fa_fwd_ex(const fa_fwd_args* args);
 #define FA_MAX_SPLITS 32
 
 /* Split count the library would choose for this shape on the current device:
- * 1 (fa_fwd is better) unless the query blocks fill less than half of the SMs;
- * then about one wave of CTAs, with at least four key tiles per range. */
+ * 1 (fa_fwd is better) unless the query blocks fill less than half of the SMs,
+ * or, with causal != 0, no more than all of them (a causal wave lasts as long
+ * as its longest block); then about one wave of CTAs, with at least four key
+ * tiles per range. */
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal);
 
 /* The split count fa_fwd_ex chooses for num_splits = 0 with these arguments:

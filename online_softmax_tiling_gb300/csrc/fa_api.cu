@@ -178,19 +178,26 @@ size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
 // of them, into about one wave of CTAs, keeping at least 512 keys per range.
 // SMs of the current device (148 if it cannot be asked).
 int sm_count() {
-    int device = 0, sms = 148;
+    int device = 0, sms = 152;  // GB300's count where no device answers
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-        sms = 148;
+        sms = 152;
     return sms;
 }
 
-int choose_splits(int64_t BH, int Nq, int Nk, int kd) {
+// Split count for num_splits = 0.  Without the mask every query block takes
+// as long as any other, so splitting pays only when the blocks leave more
+// than half of the SMs idle: up to there one wave of whole blocks is as short
+// as two waves of halves.  With the causal mask a wave lasts as long as its
+// longest block (the one that sees every key), so a grid that fits in one
+// wave is split as well: the halves of the long blocks then share CTAs with
+// the short blocks in the persistent schedule.
+int choose_splits(int64_t BH, int Nq, int Nk, int kd, bool causal) {
     if (kd == 0) return 1;
     const int sms = sm_count();
     const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
     const int64_t blocks = BH * ((Nq + block_m - 1) / block_m);
-    if (2 * blocks > sms) return 1;
+    if (blocks > sms || (!causal && 2 * blocks > sms)) return 1;
     int64_t s = (static_cast<int64_t>(sms) + blocks - 1) / blocks;
     s = std::min<int64_t>(s, std::max<int64_t>(1, static_cast<int64_t>(Nk) / 512));
     s = std::min<int64_t>(s, FA_MAX_SPLITS);
@@ -248,7 +255,8 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         misaligned(a.lse, 4))
         return FA_ERR_MISALIGNED;
     int num_splits = a.num_splits;
-    if (num_splits == 0) num_splits = choose_splits(static_cast<int64_t>(B) * H, Nq, Nk, kernel_dim(d));
+    if (num_splits == 0)
+        num_splits = choose_splits(static_cast<int64_t>(B) * H, Nq, Nk, kernel_dim(d), causal);
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
     const bool split = num_splits > 1;
     if (split) {
@@ -321,9 +329,19 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         mp.d_out = d;
         mp.rows = BH * Nq;
         void* margs[] = {&mp};
-        const dim3 mgrid(static_cast<unsigned>((mp.rows + 7) / 8));
-        if (cudaLaunchKernel(select_merge(kd, dtype), mgrid, dim3(256), margs, 0, st) != cudaSuccess)
-            return FA_ERR_CUDA;
+        // a programmatic dependent launch: the merge grid is set up while the
+        // attention kernel runs, and waits (griddepcontrol.wait) for its end
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t mcfg = {};
+        mcfg.gridDim = dim3(static_cast<unsigned>((mp.rows + 7) / 8));
+        mcfg.blockDim = dim3(256);
+        mcfg.dynamicSmemBytes = 0;
+        mcfg.stream = st;
+        mcfg.attrs = attr;
+        mcfg.numAttrs = 1;
+        if (cudaLaunchKernelExC(&mcfg, select_merge(kd, dtype), margs) != cudaSuccess) return FA_ERR_CUDA;
     }
     return FA_OK;
 }
@@ -351,14 +369,14 @@ int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* ls
 }
 
 int fa_splitkv_num_splits(int B, int H, int N, int d, int causal) {
-    (void)causal;
     if (B < 1 || H < 1 || N < 1) return 1;
-    return choose_splits(static_cast<int64_t>(B) * H, N, N, kernel_dim(d));
+    return choose_splits(static_cast<int64_t>(B) * H, N, N, kernel_dim(d), causal != 0);
 }
 
 int fa_splitkv_num_splits_ex(const fa_fwd_args* a) {
     if (!a || a->B < 1 || a->H < 1 || a->Nq < 1 || a->Nk < 1) return 1;
-    return choose_splits(static_cast<int64_t>(a->B) * a->H, a->Nq, a->Nk, kernel_dim(a->d));
+    return choose_splits(static_cast<int64_t>(a->B) * a->H, a->Nq, a->Nk, kernel_dim(a->d),
+                         a->mask != FA_MASK_NONE);
 }
 
 size_t fa_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {

@@ -775,9 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
             }
 
-            // ---- epilogue: O = U / lhat -> 16-bit, stored from registers (each
-            // thread its own row), so that Q's shared memory is free for the
-            // next unit as soon as its last S product is done
+            // ---- epilogue: O = U / lhat -> 16-bit (each thread its own row),
+            // through the warp's staging box and TMA stores; Q's shared memory
+            // is free for the next unit as soon as its last S product is done
             if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (n - 1) & 1, abort, tmo);
             if (aborted) break;
             const float l_all = lsum.x + lsum.y;
@@ -901,7 +901,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // normalised by the sum of its rounded weights, so w_s is that sum on the
 // common scale, which keeps O an exact convex combination of every weight
 // fed to P.V.  A warp per row; each lane owns D/32 consecutive columns of the
-// kernel's width D, of which the first d_out are written.
+// kernel's width D, of which the first d_out are written.  The merge is bound
+// by memory latency, not bandwidth, so a row's loads are issued before any is
+// used: lane s reads range s's two log-sums (one round trip for all ranges),
+// and the partial O rows are read four ranges at a time.
 struct MergeParams {
     const float* o_part;
     const float* lse_part;
@@ -909,46 +912,78 @@ struct MergeParams {
     long long o_sb, o_sh, o_sn;
     float* lse;                         // at lse + b lse_sb + h lse_sh + i
     long long lse_sb, lse_sh;
-    int num_splits, H, Nq;
+    int num_splits, H, Nq;              // num_splits <= 32 (one lane per range)
     int d_out;                          // columns of O written (<= D, a multiple of 8)
     long long rows;                     // B H Nq
 };
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams mp) {
     constexpr int kPer = D / 32;
+    constexpr int kBatch = 4;  // ranges whose partial rows are in flight together
+    // launched as a programmatic dependent of the attention kernel: wait until
+    // that grid has finished and its partials are visible (no-op otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const long long rows = mp.rows;
     const int num_splits = mp.num_splits;
-    const float* o_part = mp.o_part;
-    const float* lse_part = mp.lse_part;
-    if (r >= rows) return;
+    if (r >= rows) return;  // whole warps: the shuffles below see all 32 lanes
     const long long bh = r / mp.Nq, i = r % mp.Nq;
     const long long b = bh / mp.H, h = bh % mp.H;
     const size_t plane = static_cast<size_t>(num_splits) * rows;
-    float mh = -INFINITY, ml = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) {
-        mh = fmaxf(mh, lse_part[plane + s * rows + r]);
-        ml = fmaxf(ml, lse_part[s * rows + r]);
-    }
+    const float ls = lane < num_splits ? mp.lse_part[lane * rows + r] : -INFINITY;
+    const float lh = lane < num_splits ? mp.lse_part[plane + lane * rows + r] : -INFINITY;
+    const float ml = warp_max(ls), mh = warp_max(lh);
+    // an empty range (-inf) has no weight and wrote no O row
+    const float lsum = warp_sum(ls == -INFINITY ? 0.f : __expf(ls - ml));
+    const float w = lh == -INFINITY ? 0.f : __expf(lh - mh);
+    const float wsum = warp_sum(w);
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-    float wsum = 0.f, lsum = 0.f;
-    for (int s = 0; s < num_splits; ++s) {
-        const float lh = lse_part[plane + s * rows + r];
-        lsum += (ml == -INFINITY) ? 0.f : __expf(lse_part[s * rows + r] - ml);
-        if (lh == -INFINITY) continue;  // empty range: no weight, O_s not written
-        const float w = __expf(lh - mh);
-        wsum += w;
-        const float* src = o_part + (s * rows + r) * D + lane * kPer;
+    const float* src = mp.o_part + r * D + lane * kPer;
+    for (int s0 = 0; s0 < num_splits; s0 += kBatch) {
+        float ws[kBatch], v[kBatch][kPer];
 #pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-            const float2 v = *reinterpret_cast<const float2*>(src + e);
-            acc[e] = fmaf(w, v.x, acc[e]);
-            acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        for (int j = 0; j < kBatch; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);
+            ws[j] = s0 + j < num_splits ? wj : 0.f;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) v[j][e] = 0.f;
+            if (ws[j] > 0.f) {
+                const float* row_s = src + static_cast<size_t>(s0 + j) * rows * D;
+                if constexpr (kPer % 4 == 0) {
+#pragma unroll
+                    for (int e = 0; e < kPer; e += 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(row_s + e);
+                        v[j][e] = x.x; v[j][e + 1] = x.y; v[j][e + 2] = x.z; v[j][e + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kPer; e += 2) {
+                        const float2 x = *reinterpret_cast<const float2*>(row_s + e);
+                        v[j][e] = x.x; v[j][e + 1] = x.y;
+                    }
+                }
+            }
         }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] = fmaf(ws[j], v[j][e], acc[e]);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint32_t packed[kPer / 2];

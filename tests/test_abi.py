@@ -107,6 +107,26 @@ def test_splitkv_workspace_size_and_validation(lib):
     assert fa.fa_splitkv_num_splits(1, 1, 4096, 100, 0) == 1      # unsupported d: no split
 
 
+def test_split_heuristic_by_mask():
+    """With 152 SMs (GB300; also the count used where no device answers): 128
+    query blocks of 256 rows fill one wave.  Unmasked, two waves of halves are
+    no shorter, so no split; causal, the wave is as long as its longest block,
+    so its key range is halved.  Beyond one wave neither splits."""
+    import online_softmax_tiling_gb300 as fa
+    try:
+        import torch
+        if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
+            pytest.skip("the counts below assume 152 SMs")
+    except ImportError:
+        pass
+    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 0) == 1
+    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 1) == 2
+    assert fa.fa_splitkv_num_splits(1, 10, 4000, 128, 1) == 1     # 160 blocks > 152
+    assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 0) == 5      # 32 blocks: about one wave
+    assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 1) == 5
+    assert fa.fa_splitkv_num_splits(1, 8, 1024, 128, 1) == 2      # 32 blocks, but two ranges of 4 key tiles at most
+
+
 @pytest.mark.parametrize("d,width", [(8, 64), (64, 64), (72, 128), (96, 128), (128, 128),
                                      (136, 192), (192, 192), (200, 256), (256, 256)])
 def test_splitkv_workspace_uses_the_kernel_width(lib, d, width):
