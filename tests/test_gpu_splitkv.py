@@ -30,6 +30,7 @@ CASES = [  # (B, H, N, d, dtype, causal, num_splits); 0 = the library's choice
     (1, 1, 129, 128, synth.FP16, True, 32),    # mostly empty ranges
     (1, 1, 64, 64, synth.FP16, False, 2),      # one key tile, one empty range
     (1, 3, 2048, 128, synth.FP16, True, 5),
+    (1, 8, 4000, 128, synth.BF16, True, 0),    # causal, one wave of blocks: the library splits it
 ]
 
 
