@@ -49,8 +49,8 @@ EncodeTiledFn encode_fn() {
 // of one head are out of range (zero-filled on load, clipped on store)
 // instead of belonging to the next head.  Columns >= d are out of range too:
 // a kernel wider than d reads zeros there and never writes them.  Box: 64
-// columns (128 bytes, one swizzle span) x box_rows rows (one query tile or
-// one key tile) x 1 x 1.
+// columns (128 bytes, one swizzle span) x box_rows rows (a query or key tile,
+// one part of a V tile, or the 32 rows of O one softmax warp stores) x 1 x 1.
 bool encode_4d(CUtensorMap* map, const void* ptr, int dtype, int64_t B, int64_t H, int64_t rows,
                int64_t d, const long long (&stride)[3], uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
@@ -172,26 +172,25 @@ size_t split_workspace_bytes(int64_t S, int64_t BH, int64_t N, int64_t d) {
     return split_o_bytes(S, BH, N, d) + static_cast<size_t>(2 * S * BH * N) * 4;
 }
 
-// Split count for BH heads of Nq query rows and Nk keys on a kernel of
-// width kd.  Splitting pays for its fp32 partials and merge only when most
-// SMs would otherwise idle: split when the query blocks fill less than half
-// of them, into about one wave of CTAs, keeping at least 512 keys per range.
-// SMs of the current device (148 if it cannot be asked).
+// SMs of the current device (GB300's 152 if it cannot be asked).
 int sm_count() {
-    int device = 0, sms = 152;  // GB300's count where no device answers
+    int device = 0, sms = 152;
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         sms = 152;
     return sms;
 }
 
-// Split count for num_splits = 0.  Without the mask every query block takes
-// as long as any other, so splitting pays only when the blocks leave more
-// than half of the SMs idle: up to there one wave of whole blocks is as short
-// as two waves of halves.  With the causal mask a wave lasts as long as its
-// longest block (the one that sees every key), so a grid that fits in one
-// wave is split as well: the halves of the long blocks then share CTAs with
-// the short blocks in the persistent schedule.
+// Split count for num_splits = 0: BH heads of Nq query rows and Nk keys on
+// a kernel of width kd.  Splitting costs fp32 partials and a merge.  Without
+// the mask every query block takes as long as any other, so splitting pays
+// only when the blocks leave more than half of the SMs idle: up to there one
+// wave of whole blocks is as short as two waves of halves.  With the causal
+// mask a wave lasts as long as its longest block (the one that sees every
+// key), so a grid that fits in one wave is split as well: the halves of the
+// long blocks then share CTAs with the short blocks in the persistent
+// schedule.  The count aims at about one wave of CTAs, with at least 512 keys
+// per range.
 int choose_splits(int64_t BH, int Nq, int Nk, int kd, bool causal) {
     if (kd == 0) return 1;
     const int sms = sm_count();
