@@ -917,16 +917,17 @@ struct MergeParams {
     long long rows;                     // B H Nq
 };
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+// Maximum and sum over lanes [0, n) of a warp (n <= 32; the other lanes of
+// each aligned group of the next power of two >= n hold the identity), given
+// to every lane: butterfly steps below that power of two, then lane 0's value.
+__device__ __forceinline__ float lanes_max(float v, int n) {
+    for (int o = 1; o < n; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return __shfl_sync(0xffffffffu, v, 0);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+__device__ __forceinline__ float lanes_sum(float v, int n) {
+    for (int o = 1; o < n; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return __shfl_sync(0xffffffffu, v, 0);
 }
 
 template <int D, bool BF16>
@@ -941,16 +942,28 @@ __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams m
     const long long rows = mp.rows;
     const int num_splits = mp.num_splits;
     if (r >= rows) return;  // whole warps: the shuffles below see all 32 lanes
-    const long long bh = r / mp.Nq, i = r % mp.Nq;
-    const long long b = bh / mp.H, h = bh % mp.H;
+    // (b, h, i) of the row, in 32-bit arithmetic where it fits (a 64-bit
+    // division costs about as many instructions as the rest of the row)
+    long long bh, i;
+    if (rows <= 0x7fffffffll) {
+        const unsigned ru = static_cast<unsigned>(r), nq = static_cast<unsigned>(mp.Nq);
+        const unsigned qu = ru / nq;
+        bh = qu;
+        i = ru - qu * nq;
+    } else {
+        bh = r / mp.Nq;
+        i = r - bh * mp.Nq;
+    }
+    const unsigned hu = static_cast<unsigned>(mp.H), bu = static_cast<unsigned>(bh) / hu;  // BH < 2^31
+    const long long b = bu, h = static_cast<unsigned>(bh) - bu * hu;
     const size_t plane = static_cast<size_t>(num_splits) * rows;
     const float ls = lane < num_splits ? mp.lse_part[lane * rows + r] : -INFINITY;
     const float lh = lane < num_splits ? mp.lse_part[plane + lane * rows + r] : -INFINITY;
-    const float ml = warp_max(ls), mh = warp_max(lh);
+    const float ml = lanes_max(ls, num_splits), mh = lanes_max(lh, num_splits);
     // an empty range (-inf) has no weight and wrote no O row
-    const float lsum = warp_sum(ls == -INFINITY ? 0.f : __expf(ls - ml));
+    const float lsum = lanes_sum(ls == -INFINITY ? 0.f : __expf(ls - ml), num_splits);
     const float w = lh == -INFINITY ? 0.f : __expf(lh - mh);
-    const float wsum = warp_sum(w);
+    const float wsum = lanes_sum(w, num_splits);
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
