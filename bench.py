@@ -516,15 +516,28 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0))
     BH = w.B * w.H
     rows_per_step = args.ref_rows
+    t_warm = 0.0
     for s in range(args.warmup):
+        t0 = time.perf_counter()
         oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal,
                                 synth.sample_rows(BH, w.N, rows_per_step, 900 + s, False),
                                 nthreads=cores)
+        t_warm += time.perf_counter() - t0
+    # each step a bounded sample: the timed steps together take about
+    # --ref-seconds whatever --steps is (the rate, not the sample, is
+    # reported).  The oracle hands its threads 16 rows at a time, so a
+    # smaller sample keeps fewer threads busy: a row then costs about the
+    # warm-up's time per row times the thread count, and only the threads the
+    # sample can occupy are started (and reported).
+    per_row = t_warm / (args.warmup * rows_per_step)
+    if args.steps * rows_per_step * per_row > args.ref_seconds:
+        rows_per_step = max(1, int(args.ref_seconds / (args.steps * per_row * cores)))
+    threads = max(1, min(cores, -(-rows_per_step // 16)))
     flops, t = 0.0, 0.0
     for s in range(args.steps):
         rows = synth.sample_rows(BH, w.N, rows_per_step, 1900 + s, False)
         t0 = time.perf_counter()
-        oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, rows, nthreads=cores)
+        oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal, rows, nthreads=threads)
         t += time.perf_counter() - t0
         flops += _row_flops(w, rows)
     value = flops / t / 1e12
@@ -535,7 +548,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), SplitMix64 + Box-Muller)",
         "config": {**w.describe(), "parallelism": "host cores (oracle)"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{rows_per_step} seeded query rows per step of {w.name}"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -559,7 +572,10 @@ def main(argv=None):
                     help="naive: the step-by-step baseline with S and P in HBM")
     ap.add_argument("--no-ceilings", action="store_true",
                     help="skip the exp-rate and L2-bandwidth microbenchmarks")
-    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-rows", type=int, default=256,
+                    help="--impl reference: at most this many query rows per step")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: about this long for all timed steps together")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
