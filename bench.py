@@ -523,15 +523,21 @@ def run_reference(args):
                                 synth.sample_rows(BH, w.N, rows_per_step, 900 + s, False),
                                 nthreads=cores)
         t_warm += time.perf_counter() - t0
-    # each step a bounded sample: the timed steps together take about
+    # each step a bounded sample: the timed steps together take at most about
     # --ref-seconds whatever --steps is (the rate, not the sample, is
-    # reported).  The oracle hands its threads 16 rows at a time, so a
-    # smaller sample keeps fewer threads busy: a row then costs about the
-    # warm-up's time per row times the thread count, and only the threads the
-    # sample can occupy are started (and reported).
-    per_row = t_warm / (args.warmup * rows_per_step)
-    if args.steps * rows_per_step * per_row > args.ref_seconds:
-        rows_per_step = max(1, int(args.ref_seconds / (args.steps * per_row * cores)))
+    # reported).  The oracle hands its threads 16 rows at a time, so a step of
+    # r rows lasts as long as one thread's share of 16-row chunks: the largest
+    # r that fits is kept, and only the threads it keeps busy are started
+    # (and reported).
+    def chunks_per_thread(r):
+        return -(-(-(-r // 16)) // cores)
+
+    def step_rows(r):  # rows one thread works through in a step of r rows
+        return r if r < 16 else 16 * chunks_per_thread(r)
+
+    t_row = t_warm / args.warmup / step_rows(rows_per_step)  # one row on one thread
+    while rows_per_step > 1 and args.steps * step_rows(rows_per_step) * t_row > args.ref_seconds:
+        rows_per_step -= 16 if rows_per_step > 16 else 1
     threads = max(1, min(cores, -(-rows_per_step // 16)))
     flops, t = 0.0, 0.0
     for s in range(args.steps):
@@ -574,8 +580,8 @@ def main(argv=None):
                     help="skip the exp-rate and L2-bandwidth microbenchmarks")
     ap.add_argument("--ref-rows", type=int, default=256,
                     help="--impl reference: at most this many query rows per step")
-    ap.add_argument("--ref-seconds", type=float, default=60.0,
-                    help="--impl reference: about this long for all timed steps together")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: at most about this long for all timed steps together")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
