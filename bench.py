@@ -114,7 +114,8 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed
+    region (the fallback where NVML cannot be loaded in-process)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -148,7 +149,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "source": "nvidia-smi"}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -172,7 +174,120 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi -lms 50"}
+
+
+class NvmlClocks:
+    """In-process clock record through NVML's read-only queries (ctypes on
+    libnvidia-ml): the SM clock, its maximum, the power draw and the active
+    clock-event (throttle) reasons, sampled by a thread about once per
+    millisecond plus once at the start and the end of each timed region, so
+    that even a region of a few milliseconds has samples.  The device is found
+    by the PCI bus id of the CUDA device (NVML numbers every GPU of the
+    machine, CUDA only the visible ones).  Nothing is ever set."""
+
+    CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device: int):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        props = torch.cuda.get_device_properties(torch_device)
+        self.handle = ctypes.c_void_p()
+        ok = False
+        if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle)) == 0
+        if not ok:
+            idx = torch_device
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            if vis and vis.split(",")[0].strip().isdigit():
+                idx = int(vis.split(",")[torch_device].strip())
+            if lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.handle)) != 0:
+                raise OSError("no NVML handle for the CUDA device")
+        self.lib = lib
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, self.CLOCK_SM, ctypes.byref(mx)) == 0 else None)
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def sample(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, self.CLOCK_SM, ct.byref(mhz)) != 0:
+            return
+        p = float(mw.value) / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw)) == 0 \
+            else None
+        r = int(rs.value) if self._reasons_fn(self.handle, ct.byref(rs)) == 0 else 0
+        self.samples.append((float(mhz.value), p, r))
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.sample()
+            time.sleep(0.001)
+
+    def start(self):
+        self.samples = []
+        self._stop.clear()
+        self.sample()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        self.sample()
+        sm = [s[0] for s in self.samples]
+        pw = [s[1] for s in self.samples if s[1] is not None]
+        reasons = set()
+        for _, _, r in self.samples:
+            reasons |= {nm for bit, nm in self.REASONS.items() if r & bit}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(pw) if pw else None, "samples": len(sm),
+                "reasons": sorted(reasons), "source": "NVML in-process, ~1 kHz"}
+
+
+def clock_sampler(torch_device: int):
+    """NVML in-process where it loads, else nvidia-smi."""
+    try:
+        return NvmlClocks(torch_device)
+    except (OSError, AttributeError, TypeError):
+        return ClockSampler(torch_device)
+
+
+def time_launches(step, stream, n: int, flush_buf=None):
+    """CUDA-event times (ms) of n launches of `step` on `stream`: back to back
+    (an event between consecutive launches), or with L2 flushed before each
+    launch (a fill of flush_buf, outside the timed launch)."""
+    import torch
+    if flush_buf is None:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        evs[0].record(stream)
+        for i in range(n):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(n)]
+    for a, b in pairs:
+        flush_buf.fill_(1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in pairs]
 
 
 L2_BYTES = 129 * 10 ** 6
@@ -297,42 +412,25 @@ def run_ours(args):
     # flushed (a 256 MiB fill, outside the timed launches) before every step
     flush = w.compulsory_bytes < 2 * L2_BYTES
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    if flush:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for a, b in evs:
-            flush_buf.fill_(1)
-            a.record(stream)
-            step()
-            b.record(stream)
-    else:
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-    torch.cuda.synchronize()
+    # every launch between two events on its stream: the sum is the timed
+    # region (back to back), the median the typical launch
+    per_launch = time_launches(step, stream, args.steps, flush_buf)
     wall_ms = (time.perf_counter() - t_wall) * 1e3
     barrier(world)
     clock_info = clocks.stop()
-    dev_ms = sum(a.elapsed_time(b) for a, b in evs) if flush else ev0.elapsed_time(ev1)
+    dev_ms = sum(per_launch)
+    median_ms = statistics.median(per_launch)
     del flush_buf
     # with L2 flushed before every step, also the warm figure: the same steps
     # back to back, inputs left in L2 by the previous step
     warm_ms = None
     if flush:
-        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0.record(stream)
-        for _ in range(args.steps):
-            step()
-        w1.record(stream)
-        torch.cuda.synchronize()
-        warm_ms = w0.elapsed_time(w1) / args.steps
+        warm_ms = statistics.median(time_launches(step, stream, args.steps))
     if fa.fa_check_device_status(sptr) != fa.FA_OK:
         raise RuntimeError("device status not OK after the timed region")
     ms_total = max_over_ranks(dev_ms, world)
@@ -445,6 +543,20 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, q_h, k_h, v_h, budget_s=args.cpu_seconds)
 
+    # every configured workload at its full size (rank 0; outside the timed
+    # region above, which is the headline), with parity of sampled rows
+    configs = None
+    if rank == 0 and args.configs and not naive:
+        del q, k, v, o, lse, ws
+        torch.cuda.empty_cache()
+        fbuf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        configs = []
+        for name in [c for c in args.configs.split(",") if c]:
+            configs.append(sweep_config(name, fa, torch, peak, fbuf,
+                                        with_parity=not args.no_cpu_baseline))
+            torch.cuda.empty_cache()
+        del fbuf
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
@@ -466,15 +578,92 @@ def run_ours(args):
                     "steps": e2e_steps, "timing": "host wall clock around synchronised steps",
                     "pipelining": "2 buffer sets; H2D, compute, D2H on three streams"},
             "gpu_launches": args.steps * launches_per_step,
+            "median_ms_per_launch": round(median_ms, 5),
+            "kcycles_per_launch": (round(median_ms * clock_info["sm_mhz"], 1)
+                                   if clock_info.get("sm_mhz") else None),
             "clocks": clock_info,
             "ceilings": ceilings,
             "wall_ms_timed_region": round(wall_ms, 3),
             "cpu_baseline": cpu,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+SWEEP = ("C1", "C2", "C3", "C4", "C5", "C5r", "T_b2h32n4096d128_fp16", "T_b2h32n4096d128_bf16")
+
+
+def sweep_config(name: str, fa, torch, peak: float, flush_buf, with_parity: bool,
+                 seconds: float = 0.25) -> dict:
+    """One workload at its full size, on the library's own split choice:
+    the median per-launch time with L2 flushed before every launch and with
+    launches back to back (warm), TFLOP/s and % of peak from the flushed
+    median, the clock record of those launches, and (with_parity) the parity
+    statistics of sampled rows against the oracle."""
+    w = synth.workload(name)
+    B, H, N, d = w.shape
+    q_h, k_h, v_h = synth.make_inputs(w)
+    tdt = torch.float16 if w.dtype == synth.FP16 else torch.bfloat16
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(tdt).cuda()
+
+    q, k, v = dev(q_h), dev(k_h), dev(v_h)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    splits = fa.fa_splitkv_num_splits(B, H, N, d, int(w.causal))
+    ws_bytes = fa.fa_splitkv_workspace_size(B, H, N, d, splits) if splits > 1 else 0
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+
+    def step():
+        if splits > 1:
+            st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, w.scale, int(w.causal), w.dtype,
+                                   splits, ws.data_ptr(), ws_bytes, sptr)
+        else:
+            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, H, N, d, w.scale, int(w.causal), w.dtype, sptr)
+        if st != fa.FA_OK:
+            raise fa.FaError(st)
+
+    for _ in range(3):
+        step()
+    one = statistics.median(time_launches(step, stream, 3))
+    if fa.fa_check_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError(f"{name}: device status not OK after warm-up")
+    n = int(min(300, max(20, seconds / (one * 1e-3))))
+    clocks = clock_sampler(torch.cuda.current_device())
+    clocks.start()
+    flushed = time_launches(step, stream, n, flush_buf)
+    warm = time_launches(step, stream, n)
+    ci = clocks.stop()
+    if fa.fa_check_device_status(sptr) != fa.FA_OK:
+        raise RuntimeError(f"{name}: device status not OK after the timed launches")
+    mf, mw = statistics.median(flushed), statistics.median(warm)
+    tf = w.flops / (mf * 1e-3) / 1e12
+    out = {"workload": w.name, "num_splits": splits, "launches": n,
+           "launches_per_call": 2 if splits > 1 else 1,
+           "median_ms_flushed": round(mf, 5), "median_ms_warm": round(mw, 5),
+           "tflops": round(tf, 2), "tflops_warm": round(w.flops / (mw * 1e-3) / 1e12, 2),
+           "pct_of_peak": round(100 * tf / peak, 2),
+           "sm_mhz": ci.get("sm_mhz"), "clock_samples": ci.get("samples"),
+           "clock_reasons": ci.get("reasons"),
+           "kcycles_per_launch": (round(mf * ci["sm_mhz"], 1) if ci.get("sm_mhz") else None)}
+    if with_parity:
+        rows = synth.sample_rows(B * H, N, 256, w.seed_base + 9)
+        if w.causal:   # the first rows see the fewest keys
+            rows = np.unique(np.concatenate([rows, np.arange(min(N, 128), dtype=np.int64)]))
+        rt = torch.from_numpy(rows).cuda()
+        o_rows = o.view(-1, d).index_select(0, rt).view(torch.int16).cpu().numpy().view(np.uint16)
+        lse_rows = lse.view(-1).index_select(0, rt).cpu().numpy()
+        out["parity"] = cpu_leg_parity(w, q_h, k_h, v_h, rows, o_rows, lse_rows)
+    del q, k, v, o, lse, ws
+    return out
 
 
 # --------------------------------------------------------- oracle timing
@@ -504,6 +693,30 @@ def cpu_baseline(w, q_h, k_h, v_h, budget_s: float = 10.0):
             "kind": "oracle",
             "sample": f"{nrows} seeded query rows (all their keys) of {w.name}, fp64, "
                       f"{total_t:.1f} s on {cores} host threads"}
+
+
+def cpu_leg_parity(w, q_h, k_h, v_h, rows, o_rows, lse_rows) -> dict:
+    """Part of the CPU-baseline leg: the oracle (as it stands) on sampled rows
+    of one workload, timed on the host cores; its outputs are the parity
+    reference for the same rows of the GPU run, gated as the tests gate them
+    (error beyond half an output ulp: max <= 4e-3, mean <= 5e-4; LSE error
+    <= 1e-4 relative to max(1, |LSE|))."""
+    import oracle
+    from tests import parity
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    o_ref, lse_ref, spread = oracle.attention_rows16(q_h, k_h, v_h, w.dtype, w.scale, w.causal,
+                                                     rows, nthreads=cores, with_spread=True)
+    t = time.perf_counter() - t0
+    st = parity.compare(o_rows, lse_rows, o_ref, lse_ref, spread, w.dtype)
+    st["pass"] = bool(st["finite"] and st["excess_max"] <= parity.MAX_EXCESS
+                      and st["excess_mean"] <= parity.MEAN_EXCESS
+                      and st["lse_rel_max"] <= parity.LSE_REL)
+    st["rows"] = int(rows.size)
+    st["oracle_s"] = round(t, 3)
+    st["oracle_tflops"] = round(_row_flops(w, rows) / t / 1e12, 6)
+    st["oracle_cores"] = cores
+    return {k_: (float(f"{v_:.4g}") if isinstance(v_, float) else v_) for k_, v_ in st.items()}
 
 
 def run_reference(args):
@@ -578,6 +791,9 @@ def main(argv=None):
                     help="naive: the step-by-step baseline with S and P in HBM")
     ap.add_argument("--no-ceilings", action="store_true",
                     help="skip the exp-rate and L2-bandwidth microbenchmarks")
+    ap.add_argument("--configs", default=",".join(SWEEP),
+                    help="workloads timed one by one after the headline (comma-separated; "
+                         "empty = none), each with sampled-row parity against the oracle")
     ap.add_argument("--ref-rows", type=int, default=256,
                     help="--impl reference: at most this many query rows per step")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

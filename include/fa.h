@@ -176,14 +176,23 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * point keeps the partials in a fixed array of FA_NOALLOC_SCRATCH_BYTES inside
  * the library, which every GPU that loads the library holds until exit; it
  * calls no cudaMalloc, cudaFree or other allocating routine.
- * Arguments as fa_fwd_splitkv without the workspace.  Returns
- * FA_ERR_UNSUPPORTED when fa_splitkv_workspace_size() of the request is above
- * FA_NOALLOC_SCRATCH_BYTES (use fa_fwd_splitkv with a workspace instead).
+ * Arguments as fa_fwd_splitkv without the workspace, checked in the same
+ * order as every other entry point (FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED
+ * for d, FA_ERR_MISALIGNED before any size rule of the array).
+ * num_splits      : 1 = plain fa_fwd (the array is not used); 2..FA_MAX_SPLITS
+ *                   = that many ranges, FA_ERR_UNSUPPORTED when
+ *                   fa_splitkv_workspace_size() of that count is above
+ *                   FA_NOALLOC_SCRATCH_BYTES (use fa_fwd_splitkv with a
+ *                   workspace instead); 0 = fa_splitkv_num_splits(), lowered
+ *                   until the partials fit the array (down to 1 = fa_fwd),
+ *                   so the library's own choice is never refused.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array and its contents
- * persist from call to call; calls that may overlap on the GPU race, so order
- * them (one stream, or events).
+ * (cudaGetSymbolAddress) with that device current and keeps it for the
+ * process; make that first call before any stream capture.  cudaDeviceReset
+ * unloads the library's device code, so the kept address is stale afterwards:
+ * do not call this entry point after resetting a device it has run on.  All
+ * calls share the one array and its contents persist from call to call; calls
+ * that may overlap on the GPU race, so order them (one stream, or events).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -209,7 +218,10 @@ int fa_version(void);
  * fa_fwd_debug - fa_fwd with testing controls; not for production use.
  * fault_mode : 0 = none; 1 = the loader never issues the first key tile, so
  *              the tensor-core warp's wait for it must time out, set
- *              FA_ERR_TIMEOUT and let every CTA exit cleanly.
+ *              FA_ERR_TIMEOUT and let every CTA exit cleanly; 2 = the launch
+ *              step reports failure instead of launching (the call returns
+ *              FA_ERR_CUDA, as for a failed cudaLaunchKernel, and nothing is
+ *              enqueued).
  * timeout_s  : limit of every pipeline wait, in seconds (> 0; fa_fwd uses 2 s).
  */
 int fa_fwd_debug(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -213,16 +213,29 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype} (float16 or bfloat16)")
 
 
+def _checked(stream_handle, what: str):
+    """Wait for the stream and raise FaError if a kernel reported a status."""
+    st = fa_check_device_status(stream_handle)
+    if st != FA_OK:
+        raise FaError(st, what)
+
+
 def attention_forward(q, k, v, scale: float | None = None, causal: bool = False, out=None,
-                      lse=None, stream=None, num_splits: int = 1):
+                      lse=None, stream=None, num_splits: int = 1, check: bool = False):
     """O, LSE for contiguous CUDA tensors q, k, v of shape [B, H, N, d].
 
     scale defaults to 1/sqrt(d).  Outputs are allocated with torch unless
     given.  num_splits: 1 = one fused launch (fa_fwd); 0 = let the library
     choose a split-KV count for shapes that cannot fill the GPU; >= 2 = that
     many key ranges (fa_fwd_splitkv, with a workspace allocated by torch).
-    Raises FaError on any non-OK status.  Asynchronous on `stream` (default:
-    torch's current stream).
+    Raises FaError on any non-OK status of the call.  Asynchronous on
+    `stream` (default: torch's current stream).
+
+    IMPORTANT: a kernel whose pipeline wait runs out of time (2 s) leaves its
+    outputs unwritten and reports FA_ERR_TIMEOUT only through the device
+    status word.  With check=True this call synchronises the stream and raises
+    FaError if that happened; otherwise the caller must call
+    fa_check_device_status() before trusting the outputs.
     """
     import torch
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
@@ -253,18 +266,22 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
                             ws.data_ptr(), nbytes, handle)
     if st != FA_OK:
         raise FaError(st)
+    if check:
+        _checked(handle, "fa_fwd")
     return out, lse
 
 
 def attention_forward_ex(q, k, v, scale: float | None = None, mask: int = FA_MASK_NONE,
-                         out=None, lse=None, stream=None, num_splits: int = 1):
+                         out=None, lse=None, stream=None, num_splits: int = 1,
+                         check: bool = False):
     """General form for CUDA tensors q [B, H, Nq, d], k, v [B, H, Nk, d] of any
     strides with d contiguous (e.g. transposed views of [B, N, H, d] data).
 
     mask: FA_MASK_NONE, FA_MASK_CAUSAL_TOP_LEFT or FA_MASK_CAUSAL_BOTTOM_RIGHT.
     out (O, [B, H, Nq, d]) and lse ([B, H, Nq], rows contiguous) may be strided
-    too; they are allocated contiguous when not given.  num_splits as in
-    attention_forward.
+    too; they are allocated contiguous when not given.  num_splits and check
+    as in attention_forward (without check, call fa_check_device_status()
+    before trusting the outputs).
     """
     import torch
     if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
@@ -305,6 +322,8 @@ def attention_forward_ex(q, k, v, scale: float | None = None, mask: int = FA_MAS
     st = fa_fwd_ex(a)
     if st != FA_OK:
         raise FaError(st, "fa_fwd_ex")
+    if check:
+        _checked(a.stream, "fa_fwd_ex")
     return out, lse
 
 

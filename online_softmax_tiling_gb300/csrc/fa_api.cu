@@ -223,23 +223,34 @@ fa_fwd_args contiguous_args(const void* q, const void* k, const void* v, void* o
     return a;
 }
 
-int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
-    const int B = a.B, H = a.H, Nq = a.Nq, Nk = a.Nk, d = a.d, dtype = a.dtype;
+bool misaligned(const void* ptr, uintptr_t al) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (al - 1)) != 0;
+}
+
+// Testing controls of fa_fwd_debug (FA_OK in production calls).
+enum FaultMode : int {
+    kFaultNone = 0,
+    kFaultSkipFirstKeyTile = 1,  // the loader never issues the first key tile: a wait times out
+    kFaultLaunch = 2,            // the launch step reports failure instead of launching
+};
+
+// Every check that does not depend on the split count: pointers, sizes,
+// dtype, scale, mask, strides and alignment.
+int check_args(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     if (!a.q || !a.k || !a.v || !a.o || !a.lse) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (a.B < 1 || a.H < 1 || a.Nq < 1 || a.Nk < 1) return FA_ERR_INVALID_ARG;
+    if (a.dtype != FA_FP16 && a.dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(a.scale) || !(a.scale > 0.f)) return FA_ERR_INVALID_ARG;
     if (a.mask != FA_MASK_NONE && a.mask != FA_MASK_CAUSAL_TOP_LEFT &&
         a.mask != FA_MASK_CAUSAL_BOTTOM_RIGHT)
         return FA_ERR_INVALID_ARG;
     if (!(timeout_s > 0.0) || !std::isfinite(timeout_s)) return FA_ERR_INVALID_ARG;
-    if (fault_mode < 0 || fault_mode > 1) return FA_ERR_INVALID_ARG;
-    const int kd = kernel_dim(d);
+    if (fault_mode < kFaultNone || fault_mode > kFaultLaunch) return FA_ERR_INVALID_ARG;
+    const int kd = kernel_dim(a.d);
     if (kd == 0) return FA_ERR_UNSUPPORTED;
-    const bool causal = a.mask != FA_MASK_NONE;
-    const int64_t BH = static_cast<int64_t>(B) * H;
+    const int64_t BH = static_cast<int64_t>(a.B) * a.H;
     const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
-    const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // query blocks per head
+    const int64_t nq = (static_cast<int64_t>(a.Nq) + block_m - 1) / block_m;  // query blocks per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
     // TMA: every stride a positive multiple of 16 bytes (8 16-bit elements);
     // LSE rows contiguous, its strides positive
@@ -247,12 +258,21 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         for (int i = 0; i < 3; ++i)
             if (st[i] <= 0 || st[i] % 8 != 0 || st[i] >= (1ll << 39)) return FA_ERR_MISALIGNED;
     if (a.lse_stride[0] <= 0 || a.lse_stride[1] <= 0) return FA_ERR_INVALID_ARG;
-    auto misaligned = [](const void* ptr, uintptr_t al) {
-        return (reinterpret_cast<uintptr_t>(ptr) & (al - 1)) != 0;
-    };
     if (misaligned(a.q, 16) || misaligned(a.k, 16) || misaligned(a.v, 16) || misaligned(a.o, 16) ||
         misaligned(a.lse, 4))
         return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
+    const int st_args = check_args(a, fault_mode, timeout_s);
+    if (st_args != FA_OK) return st_args;
+    const int B = a.B, H = a.H, Nq = a.Nq, Nk = a.Nk, d = a.d, dtype = a.dtype;
+    const int kd = kernel_dim(d);
+    const bool causal = a.mask != FA_MASK_NONE;
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // query blocks per head
     int num_splits = a.num_splits;
     if (num_splits == 0)
         num_splits = choose_splits(static_cast<int64_t>(B) * H, Nq, Nk, kernel_dim(d), causal);
@@ -309,6 +329,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     const dim3 grid(static_cast<unsigned>(ctas));
     const dim3 block(static_cast<unsigned>(ke.threads));
     const cudaStream_t st = static_cast<cudaStream_t>(a.stream);
+    if (fault_mode == kFaultLaunch) return FA_ERR_CUDA;  // as if cudaLaunchKernel had failed
     if (cudaLaunchKernel(ke.fn, grid, block, args, static_cast<size_t>(ke.smem), st) != cudaSuccess)
         return FA_ERR_CUDA;
     if (split) {
@@ -404,8 +425,11 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-// Device address of g_fa_noalloc_scratch on the current device, resolved on
-// the first call for that device (nullptr if the lookup fails).
+// Device address of g_fa_noalloc_scratch on the current device, looked up by
+// the first call made with that device current and kept for the process
+// (nullptr if the lookup fails).  cudaDeviceReset unloads the module, after
+// which the kept address is stale: the entry point is not for use after a
+// reset of a device it has already run on.
 void* noalloc_scratch() {
     static std::mutex mu;
     static void* addr[64] = {};
@@ -424,10 +448,21 @@ void* noalloc_scratch() {
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int N, int d, float scale, int causal, int dtype,
                            int num_splits, void* stream) {
-    if (num_splits == 0) num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
-    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
     fa_fwd_args a = contiguous_args(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, stream);
-    if (num_splits == 1) return fwd_core(a, 0, 2.0);
+    // the same argument checks, in the same order, as every other entry point
+    const int st_args = check_args(a, kFaultNone, 2.0);
+    if (st_args != FA_OK) return st_args;
+    if (num_splits < 0 || num_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+    if (num_splits == 0) {
+        // the library's choice, lowered until its partials fit the array
+        // (down to 1: plain fa_fwd, which needs no scratch at all)
+        num_splits = fa_splitkv_num_splits(B, H, N, d, causal);
+        while (num_splits > 1 &&
+               fa_splitkv_workspace_size(B, H, N, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES)
+            --num_splits;
+    }
+    if (num_splits == 1) return fwd_core(a, kFaultNone, 2.0);
+    // an explicit count whose partials do not fit is refused
     if (fa_splitkv_workspace_size(B, H, N, d, num_splits) > FA_NOALLOC_SCRATCH_BYTES)
         return FA_ERR_UNSUPPORTED;
     // Nothing in the partials needs to start at zero: every range writes both
@@ -439,7 +474,7 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
     a.num_splits = num_splits;
     a.workspace = scratch;
     a.workspace_bytes = FA_NOALLOC_SCRATCH_BYTES;
-    return fwd_core(a, 0, 2.0);
+    return fwd_core(a, kFaultNone, 2.0);
 }
 
 int fa_check_device_status(void* stream) {
@@ -541,9 +576,6 @@ int fa_naive_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (N % 8 != 0) return FA_ERR_UNSUPPORTED;
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (BH > 65535 || (N + 127) / 128 > 65535 || BH * N > INT32_MAX) return FA_ERR_INVALID_ARG;
-    auto misaligned = [](const void* ptr, uintptr_t al) {
-        return (reinterpret_cast<uintptr_t>(ptr) & (al - 1)) != 0;
-    };
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(o, 16) ||
         misaligned(lse, 4) || misaligned(workspace, 256))
         return FA_ERR_MISALIGNED;

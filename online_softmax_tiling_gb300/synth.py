@@ -25,6 +25,8 @@ Q, K, V of workload k.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -82,12 +84,26 @@ def bits_to_float(bits: np.ndarray, dtype: int) -> np.ndarray:
 
 
 def tensor_bits(seed: int, shape, dtype: int, mult: float = 1.0) -> np.ndarray:
-    """A tensor of iid N(0, mult^2) values, rounded to `dtype`, as uint16 bits."""
+    """A tensor of iid N(0, mult^2) values, rounded to `dtype`, as uint16 bits.
+
+    Element e is output e of the stream whatever the chunking, so the chunks
+    are drawn on several threads (numpy releases the GIL in its array loops)
+    with the same bits as one pass."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    for s0 in range(0, n, 2 * _CHUNK):          # chunk starts stay even: pairs stay whole
+
+    def chunk(s0):                              # chunk starts stay even: pairs stay whole
         s1 = min(n, s0 + 2 * _CHUNK)
         out[s0:s1] = round_to_bits(normals_range(seed, s0, s1) * mult, dtype)
+
+    starts = range(0, n, 2 * _CHUNK)
+    if len(starts) > 1:
+        workers = min(len(starts), os.cpu_count() or 1, 16)
+        with ThreadPoolExecutor(workers) as pool:
+            list(pool.map(chunk, starts))
+    else:
+        for s0 in starts:
+            chunk(s0)
     return out.reshape(shape)
 
 

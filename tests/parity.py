@@ -5,19 +5,31 @@ Tolerance (applied per output element):
   * the stated bounds are max |dO| <= 4e-3, mean |dO| <= 5e-4 for 16-bit O and
     |dLSE| <= 1e-4 relative for fp32 LSE;
   * O is a 16-bit value, so rounding the exact result to the output type is
-    unavoidable: the error is measured beyond half an ulp of the output type
-    ("excess");
-  * the pages prescribe rounding the weights P to the 16-bit input type before
-    the P.V product.  With O normalised by the sum of those same rounded
-    weights, a relative rounding error of at most u in every weight moves O_ic
-    by at most u / (1 - u) * sum_j P_ij |v_jc - O_ic| (the oracle's "spread").
-    The max gate is applied to the error beyond both roundings; the mean gate
-    to the error beyond the output rounding alone;
+    unavoidable: both O gates apply to the error beyond half an ulp of the
+    output type ("excess"), and nothing else is subtracted;
   * relative LSE error uses max(1, |LSE|) as the denominator (LSE can be ~0).
+
+One more rounding is prescribed by the pages: the weights P are rounded to the
+16-bit input type before the P.V product.  With O normalised by the sum of
+those same rounded weights, a relative rounding error of at most u in every
+weight moves O_ic by at most u / (1 - u) * sum_j P_ij |v_jc - O_ic| (the
+oracle's "spread").  On the configured workloads that term is far below the
+gate, and it is not used.  Inputs built to stress the running maximum (score
+ranges widened on purpose, so that a few keys dominate each row) may pass the
+plain gate on some elements by that term alone; only their tests pass a
+`Widened` gate, which checks the error beyond both roundings against 4e-3 and
+puts stated ceilings on the plain excess and on how many elements exceed 4e-3.
+
+Every comparison is appended to the JSON-lines file named by FA_PARITY_LOG,
+when that variable is set, so that one GPU run records the statistics of
+every case.
 """
 from __future__ import annotations
 
+import json
 import math
+import os
+from dataclasses import dataclass
 
 import numpy as np
 
@@ -63,15 +75,38 @@ def compare(o_bits, lse, o_ref, lse_ref, spread, dtype):
         "raw_max": float(raw.max()), "raw_mean": float(raw.mean()),
         "excess_max": float(excess.max()), "excess_mean": float(excess.mean()),
         "excess_beyond_weight_rounding_max": float(excess_p.max()),
-        "n_excess_over_max": int((excess > MAX_EXCESS).sum()),
+        "n_excess_over_max": int((excess > MAX_EXCESS).sum()), "n_elements": int(raw.size),
         "lse_rel_max": float(dl.max()), "finite": bool(np.isfinite(o).all() and
                                                         np.isfinite(lse).all()),
     }
 
 
-def assert_within(stats: dict, label: str = ""):
+@dataclass(frozen=True)
+class Widened:
+    """Gate for inputs whose score range is widened on purpose: the error
+    beyond the output rounding and the weight rounding must stay within
+    MAX_EXCESS everywhere; the plain excess may pass MAX_EXCESS, but by at
+    most `max_plain` and on at most `max_count` elements."""
+    max_plain: float
+    max_count: int
+
+
+def log_stats(stats: dict, label: str):
+    path = os.environ.get("FA_PARITY_LOG")
+    if path:
+        with open(path, "a", encoding="utf-8") as fh:
+            fh.write(json.dumps({"label": label, **stats}) + "\n")
+
+
+def assert_within(stats: dict, label: str = "", widened: Widened | None = None):
+    log_stats(stats, label)
     assert stats["finite"], f"{label}: non-finite output {stats}"
-    assert stats["excess_beyond_weight_rounding_max"] <= MAX_EXCESS, f"{label}: {stats}"
+    if widened is None:
+        assert stats["excess_max"] <= MAX_EXCESS, f"{label}: {stats}"
+    else:
+        assert stats["excess_beyond_weight_rounding_max"] <= MAX_EXCESS, f"{label}: {stats}"
+        assert stats["excess_max"] <= widened.max_plain, f"{label}: {stats}"
+        assert stats["n_excess_over_max"] <= widened.max_count, f"{label}: {stats}"
     assert stats["excess_mean"] <= MEAN_EXCESS, f"{label}: {stats}"
     assert stats["lse_rel_max"] <= LSE_REL, f"{label}: {stats}"
 
@@ -118,7 +153,7 @@ def oracle_rows(q_bits, k_bits, v_bits, dtype, scale, causal, rows):
                                    with_spread=True)
 
 
-def check_rows(q, k, v, dtype, mask, o_dev, lse_dev, label):
+def check_rows(q, k, v, dtype, mask, o_dev, lse_dev, label, widened: Widened | None = None):
     """Compare device outputs (torch, any strides) of every row with the oracle.
 
     Rows that see no key must be O = 0, LSE = -inf (the oracle's convention);
@@ -136,7 +171,7 @@ def check_rows(q, k, v, dtype, mask, o_dev, lse_dev, label):
         assert np.all(np.isneginf(lse[empty])), label
     keep = ~empty
     st = compare(o[keep], lse[keep], o_ref[keep], lse_ref[keep], spread[keep], dtype)
-    assert_within(st, label)
+    assert_within(st, label, widened)
     return st
 
 

@@ -1,13 +1,45 @@
 """The C-ABI library loads, exports what include/*.h declare, and rejects bad
-arguments on the host (no GPU needed: these paths return before any CUDA call)."""
+arguments on the host (no GPU needed: these paths return before any CUDA call).
+
+The calls below pass fake, never-dereferenced device addresses.  They are only
+made in a process that sees no GPU, so that even a regression in the checks
+could not launch a kernel on them: where this process sees a GPU, the module
+runs again in a child process with CUDA_VISIBLE_DEVICES empty and its tests
+here are skipped."""
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
 import online_softmax_tiling_gb300 as fa
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _gpu_visible() -> bool:
+    if os.environ.get("CUDA_VISIBLE_DEVICES", None) == "":
+        return False
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except ImportError:
+        return False
+
+
+GPU_VISIBLE = _gpu_visible()
+
+
+def test_validation_runs_where_no_gpu_is_visible():
+    """Where a GPU is visible, run this module's tests in a child that sees none."""
+    if not GPU_VISIBLE:
+        pytest.skip("no GPU visible: the tests below run in this process")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_abi.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
 
 
 def _declared():
@@ -23,6 +55,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
+    if GPU_VISIBLE:
+        pytest.skip("run by test_validation_runs_where_no_gpu_is_visible in a child process")
     if not os.path.exists(fa.LIBRARY):
         from online_softmax_tiling_gb300 import build
         build.build()
@@ -84,7 +118,8 @@ def test_host_validation(lib, kw, want):
 def test_debug_entry_validates_its_controls(lib):
     base = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 1, 128, 64, 0.125, 0,
             fa.FA_FP16, None)
-    assert fa.fa_fwd_debug(*base, 2, 1.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_debug(*base, 3, 1.0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_debug(*base, -1, 1.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_debug(*base, 0, 0.0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_debug(*base, 0, float("nan")) == fa.FA_ERR_INVALID_ARG
 
@@ -107,24 +142,52 @@ def test_splitkv_workspace_size_and_validation(lib):
     assert fa.fa_splitkv_num_splits(1, 1, 4096, 100, 0) == 1      # unsupported d: no split
 
 
-def test_split_heuristic_by_mask():
+def test_split_heuristic_by_mask(lib):
     """With 152 SMs (GB300; also the count used where no device answers): 128
     query blocks of 256 rows fill one wave.  Unmasked, two waves of halves are
     no shorter, so no split; causal, the wave is as long as its longest block,
     so its key range is halved.  Beyond one wave neither splits."""
-    import online_softmax_tiling_gb300 as fa
-    try:
-        import torch
-        if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
-            pytest.skip("the counts below assume 152 SMs")
-    except ImportError:
-        pass
+    # with no device visible the library counts GB300's 152 SMs
     assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 0) == 1
     assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 1) == 2
     assert fa.fa_splitkv_num_splits(1, 10, 4000, 128, 1) == 1     # 160 blocks > 152
     assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 0) == 5      # 32 blocks: about one wave
     assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 1) == 5
     assert fa.fa_splitkv_num_splits(1, 8, 1024, 128, 1) == 2      # 32 blocks, but two ranges of 4 key tiles at most
+
+
+def test_calls_without_a_device_return_fa_err_cuda(lib):
+    """A valid request on a machine whose CUDA calls fail (here: no device
+    visible) comes back as FA_ERR_CUDA from the tensor-map or launch step,
+    for every entry point that launches."""
+    assert _call() == fa.FA_ERR_CUDA
+    assert _call(causal=1, d=256, dtype=fa.FA_BF16) == fa.FA_ERR_CUDA
+    base = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, 1, 1, 128, 64, 0.125, 0,
+            fa.FA_FP16, None)
+    assert fa.fa_fwd_debug(*base, 2, 1.0) == fa.FA_ERR_CUDA     # the simulated launch failure
+    assert fa.fa_fwd_splitkv_noalloc(*base[:-1], 2, None) == fa.FA_ERR_CUDA
+
+
+def test_noalloc_validates_before_its_size_rule(lib):
+    """The no-alloc entry point checks its arguments in the order the others
+    do: a request that is both invalid and too large for the array reports
+    the invalid argument."""
+    B, H, N, d = 8, 16, 4096, 128
+    assert fa.fa_splitkv_workspace_size(B, H, N, d, 8) > fa.FA_NOALLOC_SCRATCH_BYTES
+    big = (B, H, N, d, 0.1, 0)
+    args = (A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000)
+    assert fa.fa_fwd_splitkv_noalloc(*args, *big, fa.FA_BF16, 8, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv_noalloc(None, *args[1:], *big, fa.FA_BF16, 8, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv_noalloc(*args, *big, 7, 8, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv_noalloc(*args, B, H, N, d, float("nan"), 0, fa.FA_BF16, 8, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv_noalloc(A + 8, *args[1:], *big, fa.FA_BF16, 8, None) == \
+        fa.FA_ERR_MISALIGNED
+    assert fa.fa_fwd_splitkv_noalloc(*args, B, H, N, 100, 0.1, 0, fa.FA_BF16, 8, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_splitkv_noalloc(*args, *big, fa.FA_BF16, 33, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_splitkv_noalloc(*args, *big, fa.FA_BF16, -1, None) == fa.FA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("d,width", [(8, 64), (64, 64), (72, 128), (96, 128), (128, 128),

@@ -207,3 +207,51 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     o_ref, lse_ref, spread = parity.oracle_rows(q_bits, q_bits, q_bits, dtype, 0.125, False, rows)
     parity.assert_within(parity.compare(o2.reshape(-1, d), lse2.reshape(-1), o_ref, lse_ref,
                                         spread, dtype), "after timeout")
+
+
+def test_failed_launch_reports_fa_err_cuda_and_writes_nothing():
+    """The launch step reporting failure (fa_fwd_debug fault_mode 2: the
+    library returns as it would for a failed cudaLaunchKernel) comes back as
+    FA_ERR_CUDA with nothing enqueued: O and LSE keep their canary values, the
+    device status stays FA_OK and the next call is correct."""
+    import torch
+    import online_softmax_tiling_gb300 as fa
+    B, H, N, d, dtype = 1, 2, 200, 128, synth.BF16
+    q_bits = synth.tensor_bits(81, (B, H, N, d), dtype)
+    q = parity.to_device(q_bits, dtype)
+    o = torch.full_like(q, -1000.0)
+    lse = torch.full((B, H, N), -1000.0, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for causal in (0, 1):
+        st = fa.fa_fwd_debug(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, H, N, d, 0.1, causal, dtype, s, 2, 2.0)
+        assert st == fa.FA_ERR_CUDA
+    assert fa.fa_check_device_status(s) == fa.FA_OK
+    assert bool((o.float() == -1000.0).all()) and bool((lse == -1000.0).all())
+    with pytest.raises(fa.FaError) as err:
+        raise fa.FaError(fa.FA_ERR_CUDA)
+    assert "FA_ERR_CUDA" in str(err.value)
+    o2, lse2, _ = parity.run_gpu(q_bits, q_bits, q_bits, dtype, 0.1, True)
+    rows = np.arange(B * H * N, dtype=np.int64)
+    o_ref, lse_ref, spread = parity.oracle_rows(q_bits, q_bits, q_bits, dtype, 0.1, True, rows)
+    parity.assert_within(parity.compare(o2.reshape(-1, d), lse2.reshape(-1), o_ref, lse_ref,
+                                        spread, dtype), "after a failed launch")
+
+
+def test_checked_wrapper_raises_on_a_timed_out_kernel():
+    """attention_forward(check=True) turns a device-side FA_ERR_TIMEOUT into an
+    exception instead of returning outputs that were never written."""
+    import torch
+    import online_softmax_tiling_gb300 as fa
+    B, H, N, d, dtype = 1, 1, 256, 64, synth.FP16
+    q = parity.to_device(synth.tensor_bits(91, (B, H, N, d), dtype), dtype)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert fa.fa_fwd_debug(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, 0.125, 0, dtype, s, 1, 0.05) == fa.FA_OK
+    with pytest.raises(fa.FaError) as err:
+        fa._checked(s, "fa_fwd")
+    assert err.value.status == fa.FA_ERR_TIMEOUT
+    out, _ = fa.attention_forward(q, q, q, scale=0.125, check=True)   # status cleared, then OK
+    assert torch.isfinite(out.float()).all()

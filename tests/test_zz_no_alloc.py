@@ -4,9 +4,11 @@ A plugin whose host framework owns all device memory, or a latency-critical
 path that cannot take cudaMalloc's implicit synchronisation, cannot provide a
 workspace.  fa_fwd_splitkv_noalloc keeps the partials in a fixed array inside
 the library instead.  Its output must match the workspace entry point's
-(fa_fwd_splitkv) within the tolerances the other tests use, on calls made one
-after the other (the array keeps the previous call's contents).  Collected
-last, and independent of every other test.
+(fa_fwd_splitkv) and the oracle within the tolerances the other tests use, on
+calls made one after the other (the array keeps the previous call's
+contents); the library's own split choice must never be refused, and an
+explicit count too large for the array must be.  Collected last, and
+independent of every other test.
 """
 import math
 
@@ -38,16 +40,39 @@ def _run(entry, q_bits, k_bits, v_bits, dtype, scale, causal, splits):
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
     args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-            scale, int(causal), dtype, splits)
+            scale, int(causal), dtype)
     if entry == "workspace":
         nbytes = fa.fa_splitkv_workspace_size(B, H, N, d, splits)
-        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        st = fa.fa_fwd_splitkv(*args, ws.data_ptr(), nbytes, s)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+        st = fa.fa_fwd_splitkv(*args, splits, ws.data_ptr(), nbytes, s)
+    elif entry == "plain":
+        st = fa.fa_fwd(*args, s)
     else:
-        st = fa.fa_fwd_splitkv_noalloc(*args, s)
+        st = fa.fa_fwd_splitkv_noalloc(*args, splits, s)
     assert st == fa.FA_OK, fa.fa_status_string(st)
     assert fa.fa_check_device_status(s) == fa.FA_OK
     return parity.from_device(o), lse.cpu().numpy()
+
+
+def _agree(o_a, l_a, o_b, l_b, dtype):
+    a = synth.bits_to_float(o_a, dtype).astype(np.float64)
+    b = synth.bits_to_float(o_b, dtype).astype(np.float64)
+    assert np.isfinite(b).all() and np.isfinite(l_b).all()
+    assert np.abs(a - b).max() <= parity.MAX_EXCESS
+    assert np.abs(a - b).mean() <= parity.MEAN_EXCESS
+    rel = np.abs(l_a - l_b) / np.maximum(1.0, np.abs(l_a))
+    assert rel.max() <= parity.LSE_REL
+
+
+def _against_oracle(q, k, v, dtype, scale, causal, o_bits, lse, label):
+    B, H, N, d = q.shape
+    rows = np.arange(B * H * N, dtype=np.int64)
+    if rows.size > 4096:
+        rows = synth.sample_rows(B * H, N, 2048, 4321)
+    o_ref, lse_ref, spread = parity.oracle_rows(q, k, v, dtype, scale, causal, rows)
+    st = parity.compare(o_bits.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref,
+                        spread, dtype)
+    parity.assert_within(st, label)
 
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
@@ -58,20 +83,50 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         scale = 1.0 / math.sqrt(shape[-1])
         o_ws, l_ws = _run("workspace", q, k, v, dtype, scale, causal, splits)
         o_na, l_na = _run("noalloc", q, k, v, dtype, scale, causal, splits)
-        a = synth.bits_to_float(o_ws, dtype).astype(np.float64)
-        b = synth.bits_to_float(o_na, dtype).astype(np.float64)
-        assert np.isfinite(b).all() and np.isfinite(l_na).all()
-        assert np.abs(a - b).max() <= parity.MAX_EXCESS
-        assert np.abs(a - b).mean() <= parity.MEAN_EXCESS
-        rel = np.abs(l_ws - l_na) / np.maximum(1.0, np.abs(l_ws))
-        assert rel.max() <= parity.LSE_REL
+        _agree(o_ws, l_ws, o_na, l_na, dtype)
+        _against_oracle(q, k, v, dtype, scale, causal, o_na, l_na, f"noalloc {shape} {splits}")
 
 
-def test_noalloc_rejects_requests_beyond_its_array():
+@pytest.mark.parametrize("shape,dtype,causal", [
+    ((1, 8, 4000, 128), synth.BF16, True),    # choice 2 needs 33 MB: lowered to 1 (fa_fwd)
+    ((1, 1, 4352, 128), synth.BF16, False),   # choice 8 needs 18 MB: lowered to 7
+])
+def test_noalloc_library_choice_is_never_refused(shape, dtype, causal):
+    import online_softmax_tiling_gb300 as fa
+    B, H, N, d = shape
+    chosen = fa.fa_splitkv_num_splits(B, H, N, d, int(causal))
+    assert fa.fa_splitkv_workspace_size(B, H, N, d, chosen) > fa.FA_NOALLOC_SCRATCH_BYTES
+    q, k, v = (synth.tensor_bits(7700 + N + i, shape, dtype) for i in range(3))
+    scale = 1.0 / math.sqrt(d)
+    o_pl, l_pl = _run("plain", q, k, v, dtype, scale, causal, 1)
+    for _ in range(2):                                   # two calls in a row
+        o_na, l_na = _run("noalloc", q, k, v, dtype, scale, causal, 0)
+        _agree(o_pl, l_pl, o_na, l_na, dtype)
+    _against_oracle(q, k, v, dtype, scale, causal, o_na, l_na, f"noalloc choice {shape}")
+
+
+def test_noalloc_single_range_is_plain_forward():
+    q, k, v = (synth.tensor_bits(8800 + i, (2, 3, 300, 64), synth.FP16) for i in range(3))
+    o_pl, l_pl = _run("plain", q, k, v, synth.FP16, 0.125, True, 1)
+    o_na, l_na = _run("noalloc", q, k, v, synth.FP16, 0.125, True, 1)
+    np.testing.assert_array_equal(o_pl, o_na)
+    np.testing.assert_array_equal(l_pl, l_na)
+
+
+def test_noalloc_rejects_an_explicit_count_beyond_its_array():
+    """Called on real device buffers of the full request size, so that no
+    regression of the size rule could make it launch on memory it does not
+    own; outputs keep their canary values."""
+    import torch
     import online_softmax_tiling_gb300 as fa
     B, H, N, d, splits = 8, 16, 4096, 128, 8
     assert fa.fa_splitkv_workspace_size(B, H, N, d, splits) > fa.FA_NOALLOC_SCRATCH_BYTES
-    A = 0x10000   # never dereferenced: the request is refused before any launch
-    st = fa.fa_fwd_splitkv_noalloc(A, A + 0x1000, A + 0x2000, A + 0x3000, A + 0x4000, B, H, N, d,
-                                   0.1, 0, fa.FA_BF16, splits, None)
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((B, H, N), 7.0, dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = fa.fa_fwd_splitkv_noalloc(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, 0.1, 0, fa.FA_BF16, splits, s)
     assert st == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_check_device_status(s) == fa.FA_OK
+    assert bool((o == 7.0).all()) and bool((lse == 7.0).all())
