@@ -86,9 +86,23 @@ class Widened:
     """Gate for inputs whose score range is widened on purpose: the error
     beyond the output rounding and the weight rounding must stay within
     MAX_EXCESS everywhere; the plain excess may pass MAX_EXCESS, but by at
-    most `max_plain` and on at most `max_count` elements."""
+    most `max_plain` and on at most a fraction `max_frac` of the elements."""
     max_plain: float
-    max_count: int
+    max_frac: float
+
+
+# With u = 2^-8 (bf16 weights) and a weighted spread sum_j P_ij |v_jc - O_ic|
+# of order one, the weight rounding can add about u, i.e. another 4e-3, to
+# the plain excess; the ceiling caps it there, and caps the share of elements
+# that use it at one in ten thousand.
+WIDENED = Widened(max_plain=2 * MAX_EXCESS, max_frac=1e-4)
+
+
+def gate_for(w) -> Widened | None:
+    """The gate of a configured workload: the plain one, except where Q and K
+    are drawn wider than N(0, 1) (the std-2 workload), whose rows are peaked
+    enough for the weight rounding to show."""
+    return WIDENED if w.qk_mult > 1.0 else None
 
 
 def log_stats(stats: dict, label: str):
@@ -106,7 +120,8 @@ def assert_within(stats: dict, label: str = "", widened: Widened | None = None):
     else:
         assert stats["excess_beyond_weight_rounding_max"] <= MAX_EXCESS, f"{label}: {stats}"
         assert stats["excess_max"] <= widened.max_plain, f"{label}: {stats}"
-        assert stats["n_excess_over_max"] <= widened.max_count, f"{label}: {stats}"
+        assert stats["n_excess_over_max"] <= widened.max_frac * stats["n_elements"], \
+            f"{label}: {stats}"
     assert stats["excess_mean"] <= MEAN_EXCESS, f"{label}: {stats}"
     assert stats["lse_rel_max"] <= LSE_REL, f"{label}: {stats}"
 
