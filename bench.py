@@ -45,7 +45,7 @@ _CSRC = "online_softmax_tiling_gb300/csrc/"
 # device code each timed path runs (the hash ties a committed ncu traffic
 # figure to the kernel source it was measured on)
 KERNEL_SOURCES = {
-    "fused": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh")],
+    "fused": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "fa_fwd_qtile_kernel.cuh", "sm103_ptx.cuh")],
     "wide": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "fa_fwd_wide_kernel.cuh", "sm103_ptx.cuh")],
     "naive": [_CSRC + f for f in ("fa_fwd_kernel.cuh", "naive_attention.cuh", "sm103_ptx.cuh")],
 }

@@ -9,7 +9,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("fa_api.cu", "ceilings.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa_fwd_wide_kernel.cuh", "naive_attention.cuh",
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_fwd_kernel.cuh", "fa_fwd_qtile_kernel.cuh", "fa_fwd_wide_kernel.cuh",
+                                                     "naive_attention.cuh",
                                                      "sm103_ptx.cuh")] + [
     os.path.join(ROOT, "include", f) for f in ("fa.h", "fa_ceilings.h", "fa_naive.h")]
 LIBRARY = os.path.join(HERE, "libfa_gb300.so")

@@ -20,6 +20,7 @@
 #include "../../include/fa.h"
 #include "../../include/fa_naive.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_qtile_kernel.cuh"
 #include "fa_fwd_wide_kernel.cuh"
 #include "naive_attention.cuh"
 
@@ -105,33 +106,58 @@ struct KernelEntry {
     int v_rows;   // rows of the V boxes (a tile or a part of one)
 };
 
+// The kernel that serves a request.  Widths 192 and 256 have their own
+// (one query tile per unit).  Widths 64 and 128 run units of two 128-row
+// query tiles that share every K/V tile, except causal grids whose 256-row
+// blocks fit in one wave: there units of one 128-row tile (twice as many,
+// dealt longest first) share the SMs more evenly than two-tile units or key
+// ranges do.
+enum class Kind { kTwoTile, kOneTile, kWide };
+
+int sm_count();
+
+Kind kernel_kind(int kd, bool causal, int64_t BH, int64_t Nq) {
+    if (kd > 128) return Kind::kWide;
+    const int64_t blocks = BH * ((Nq + fa::kBlockM - 1) / fa::kBlockM);
+    return (causal && blocks <= sm_count()) ? Kind::kOneTile : Kind::kTwoTile;
+}
+
+// Query rows per unit of work of a kernel kind.
+int64_t unit_rows(Kind k) { return k == Kind::kTwoTile ? fa::kBlockM : fa::kTileM; }
+
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
-KernelEntry entry() {
-    if constexpr (D <= 128)
+KernelEntry entry(Kind k) {
+    if constexpr (D <= 128) {
+        if constexpr (CAUSAL)  // one-tile units serve causal grids only
+            if (k == Kind::kOneTile)
+                return KernelEntry{
+                    reinterpret_cast<const void*>(&fa::fa_fwd_qtile_kernel<D, BF16, CAUSAL, SPLIT>),
+                    fa::QtCfg<D>::kSmemBytes, fa::kQtThreads, fa::kTileM, fa::kQtBlockN, fa::kQtBlockN};
         return KernelEntry{
             reinterpret_cast<const void*>(&fa::fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>),
             fa::Cfg<D>::kSmemBytes, fa::kThreads, fa::kBlockM, fa::kBlockN, fa::kBlockN};
-    else
+    } else {
         return KernelEntry{
             reinterpret_cast<const void*>(&fa::fa_fwd_wide_kernel<D, BF16, CAUSAL, SPLIT>),
             fa::WideCfg<D>::kSmemBytes, fa::kWideThreads, fa::kTileM, fa::kWideBlockN,
             fa::WideCfg<D>::kVPartRows};
+    }
 }
 
 template <int D, bool BF16>
-KernelEntry select_d_dtype(bool causal, bool split) {
-    if (causal) return split ? entry<D, BF16, true, true>() : entry<D, BF16, true, false>();
-    return split ? entry<D, BF16, false, true>() : entry<D, BF16, false, false>();
+KernelEntry select_d_dtype(Kind k, bool causal, bool split) {
+    if (causal) return split ? entry<D, BF16, true, true>(k) : entry<D, BF16, true, false>(k);
+    return split ? entry<D, BF16, false, true>(k) : entry<D, BF16, false, false>(k);
 }
 
 // kd: a kernel width from kernel_dim()
-KernelEntry select_kernel(int kd, int dtype, bool causal, bool split) {
+KernelEntry select_kernel(int kd, Kind k, int dtype, bool causal, bool split) {
     const bool bf = dtype == FA_BF16;
     switch (kd) {
-        case 64: return bf ? select_d_dtype<64, true>(causal, split) : select_d_dtype<64, false>(causal, split);
-        case 128: return bf ? select_d_dtype<128, true>(causal, split) : select_d_dtype<128, false>(causal, split);
-        case 192: return bf ? select_d_dtype<192, true>(causal, split) : select_d_dtype<192, false>(causal, split);
-        default: return bf ? select_d_dtype<256, true>(causal, split) : select_d_dtype<256, false>(causal, split);
+        case 64: return bf ? select_d_dtype<64, true>(k, causal, split) : select_d_dtype<64, false>(k, causal, split);
+        case 128: return bf ? select_d_dtype<128, true>(k, causal, split) : select_d_dtype<128, false>(k, causal, split);
+        case 192: return bf ? select_d_dtype<192, true>(k, causal, split) : select_d_dtype<192, false>(k, causal, split);
+        default: return bf ? select_d_dtype<256, true>(k, causal, split) : select_d_dtype<256, false>(k, causal, split);
     }
 }
 
@@ -194,7 +220,7 @@ int sm_count() {
 int choose_splits(int64_t BH, int Nq, int Nk, int kd, bool causal) {
     if (kd == 0) return 1;
     const int sms = sm_count();
-    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t block_m = unit_rows(kernel_kind(kd, causal, BH, Nq));
     const int64_t blocks = BH * ((Nq + block_m - 1) / block_m);
     if (blocks > sms || (!causal && 2 * blocks > sms)) return 1;
     int64_t s = (static_cast<int64_t>(sms) + blocks - 1) / blocks;
@@ -249,7 +275,7 @@ int check_args(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     const int kd = kernel_dim(a.d);
     if (kd == 0) return FA_ERR_UNSUPPORTED;
     const int64_t BH = static_cast<int64_t>(a.B) * a.H;
-    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const int64_t block_m = unit_rows(kernel_kind(kd, a.mask != FA_MASK_NONE, BH, a.Nq));
     const int64_t nq = (static_cast<int64_t>(a.Nq) + block_m - 1) / block_m;  // query blocks per head
     if (BH > INT32_MAX || BH * nq > INT32_MAX) return FA_ERR_INVALID_ARG;
     // TMA: every stride a positive multiple of 16 bytes (8 16-bit elements);
@@ -271,7 +297,8 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
     const int kd = kernel_dim(d);
     const bool causal = a.mask != FA_MASK_NONE;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    const int64_t block_m = kd <= 128 ? fa::kBlockM : fa::kTileM;
+    const Kind kind = kernel_kind(kd, causal, BH, Nq);
+    const int64_t block_m = unit_rows(kind);
     const int64_t nq = (static_cast<int64_t>(Nq) + block_m - 1) / block_m;  // query blocks per head
     int num_splits = a.num_splits;
     if (num_splits == 0)
@@ -285,7 +312,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         if (BH * nq * num_splits > INT32_MAX) return FA_ERR_INVALID_ARG;
     }
 
-    const KernelEntry ke = select_kernel(kd, dtype, causal, split);
+    const KernelEntry ke = select_kernel(kd, kind, dtype, causal, split);
     const uint32_t qrows = static_cast<uint32_t>(fa::kTileM);
     const uint32_t krows = static_cast<uint32_t>(ke.block_n);
     CUtensorMap tq, tk, tv, to;

@@ -143,17 +143,22 @@ def test_splitkv_workspace_size_and_validation(lib):
 
 
 def test_split_heuristic_by_mask(lib):
-    """With 152 SMs (GB300; also the count used where no device answers): 128
-    query blocks of 256 rows fill one wave.  Unmasked, two waves of halves are
-    no shorter, so no split; causal, the wave is as long as its longest block,
-    so its key range is halved.  Beyond one wave neither splits."""
+    """With 152 SMs (GB300; also the count used where no device answers).
+    Unmasked d = 128 runs units of two 128-row tiles: 128 of them fill one
+    wave, and two waves of halves are no shorter, so no split; 32 blocks are
+    split to about one wave.  Causal d = 128 grids whose 256-row blocks fit
+    in one wave run one-tile units instead (twice as many, longest first):
+    split only while those still fit in one wave, as a causal wave lasts as
+    long as its longest unit.  Beyond one wave nothing splits."""
     # with no device visible the library counts GB300's 152 SMs
-    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 0) == 1
-    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 1) == 2
+    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 0) == 1      # 128 blocks of 256 rows
+    assert fa.fa_splitkv_num_splits(1, 8, 4000, 128, 1) == 1      # 256 one-tile units > 152
+    assert fa.fa_splitkv_num_splits(1, 4, 4000, 128, 1) == 2      # 128 one-tile units: halved
     assert fa.fa_splitkv_num_splits(1, 10, 4000, 128, 1) == 1     # 160 blocks > 152
     assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 0) == 5      # 32 blocks: about one wave
-    assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 1) == 5
-    assert fa.fa_splitkv_num_splits(1, 8, 1024, 128, 1) == 2      # 32 blocks, but two ranges of 4 key tiles at most
+    assert fa.fa_splitkv_num_splits(1, 2, 4096, 128, 1) == 3      # 64 one-tile units
+    assert fa.fa_splitkv_num_splits(1, 8, 1024, 128, 1) == 2      # two ranges of 4 key tiles at most
+    assert fa.fa_splitkv_num_splits(1, 1, 4096, 64, 0) == 8       # 16 blocks, 8 ranges of 512 keys
 
 
 def test_calls_without_a_device_return_fa_err_cuda(lib):

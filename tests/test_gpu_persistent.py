@@ -83,3 +83,33 @@ def test_many_units_strided_views():
     fa.attention_forward_ex(qv, kv, vv, mask=1, out=ov, lse=lse)
     assert fa.fa_check_device_status(None) == fa.FA_OK
     parity.check_rows(q, k, v, dtype, 1, ov, lse, "strided causal")
+
+
+ONE_TILE_CASES = [  # (B, H, Nq, Nk, d, dtype, mask, splits): 256-row blocks fit one wave
+    (1, 76, 512, 512, 128, synth.BF16, 1, 1),     # 152 blocks -> 304 one-tile units
+    (1, 50, 520, 520, 64, synth.FP16, 1, 1),      # 150 blocks -> 250 units, ragged tail
+    (1, 60, 400, 600, 128, synth.BF16, 2, 1),     # bottom-right, more keys than queries
+    (1, 50, 700, 300, 128, synth.FP16, 2, 1),     # bottom-right: the first 400 queries see no key
+    (1, 36, 900, 900, 128, synth.BF16, 1, 2),     # one-tile units in two key ranges
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dtype,mask,splits", ONE_TILE_CASES)
+def test_many_one_tile_units_per_cta(B, H, Nq, Nk, d, dtype, mask, splits):
+    """Causal grids whose two-tile blocks fit in one wave run one 128-row
+    query tile per unit (twice as many units); here more than there are SMs."""
+    import online_softmax_tiling_gb300 as fa
+    blocks = B * H * ((Nq + 255) // 256)
+    units = B * H * ((Nq + 127) // 128) * splits
+    if blocks > _sms():
+        pytest.skip("the case assumes the one-tile kernel serves it (blocks fit in one wave)")
+    assert units > _sms(), "the shape must give some CTA more than one unit"
+    seed = 740000 + 11 * H + Nq + 3 * Nk + d + 5 * mask + splits
+    q = synth.tensor_bits(seed, (B, H, Nq, d), dtype)
+    k = synth.tensor_bits(seed + 1, (B, H, Nk, d), dtype)
+    v = synth.tensor_bits(seed + 2, (B, H, Nk, d), dtype)
+    qd, kd, vd = (parity.to_device(x, dtype) for x in (q, k, v))
+    o, lse = fa.attention_forward_ex(qd, kd, vd, mask=mask, num_splits=splits)
+    assert fa.fa_check_device_status(None) == fa.FA_OK
+    parity.check_rows(q, k, v, dtype, mask, o, lse,
+                      f"one-tile B{B} H{H} Nq{Nq} Nk{Nk} d{d} mask{mask} splits{splits}")

@@ -88,11 +88,14 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 
 
 @pytest.mark.parametrize("shape,dtype,causal", [
-    ((1, 8, 4000, 128), synth.BF16, True),    # choice 2 needs 33 MB: lowered to 1 (fa_fwd)
-    ((1, 1, 4352, 128), synth.BF16, False),   # choice 8 needs 18 MB: lowered to 7
+    ((1, 2, 8192, 128), synth.BF16, True),    # choice 2 needs 17.0 MB: lowered to 1 (fa_fwd)
+    ((1, 1, 8192, 192), synth.BF16, False),   # choice 3 needs 19.1 MB: lowered to 2
 ])
 def test_noalloc_library_choice_is_never_refused(shape, dtype, causal):
+    import torch
     import online_softmax_tiling_gb300 as fa
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the split counts in the cases assume GB300's 152 SMs")
     B, H, N, d = shape
     chosen = fa.fa_splitkv_num_splits(B, H, N, d, int(causal))
     assert fa.fa_splitkv_workspace_size(B, H, N, d, chosen) > fa.FA_NOALLOC_SCRATCH_BYTES
