@@ -113,7 +113,15 @@ struct Cfg {
     // O staging: one 32-row x 64-column swizzled box per softmax warp
     static constexpr int kOffStage = kOffV + kVStages * kTileBytes;
     static constexpr int kStageBytes = 32 * 128;
-    static constexpr int kOffCtl = kOffStage + 8 * kStageBytes;
+    // d = 64: P.V also multiplies the weights by a column of ones (16 of them,
+    // N = 80), so U carries the sum of the 16-bit weights in column 64.  The
+    // ones live in one 128-row x 64-column tile that every V slot's
+    // descriptor reaches as its second 64-column group.
+    static constexpr bool kOnes = D == 64;
+    static constexpr int kUCols = kOnes ? D + 16 : D;    // columns of U written by P.V
+    static constexpr int kOffOnes = kOffStage + 8 * kStageBytes;
+    static constexpr int kOnesBytes = kOnes ? kTileM * 128 : 0;
+    static constexpr int kOffCtl = kOffOnes + kOnesBytes;
     static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
 };
 
@@ -351,6 +359,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
+    if constexpr (C::kOnes) {
+        // the ones tile (every 16-bit element 1.0, so any swizzle of it is the
+        // same), written once and made visible to the tensor core's reads
+        constexpr uint32_t kOne2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+        uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::kOffOnes);
+        for (int i = threadIdx.x; i < C::kOnesBytes / 4; i += kThreads) ones[i] = kOne2;
+        ptx::fence_proxy_async_smem();
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -427,14 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ====================================================== tensor-core issuer
         constexpr uint32_t idesc_s = instr_desc(BF16, kTileM, kBlockN, false);
-        constexpr uint32_t idesc_pv = instr_desc(BF16, kTileM, D, true);
+        constexpr uint32_t idesc_pv = instr_desc(BF16, kTileM, C::kUCols, true);
         // stage s of a ring (and tile x of Q) is kTileBytes further on: its
         // descriptor is the first one plus that offset in 16-byte units; the
         // steps along K inside a group are built into the mma_*_k* helpers
         constexpr uint64_t kTileStep = C::kTileBytes / 16;
         const uint64_t q_desc0 = smem_desc(sQ(0), 16, 1024);
         const uint64_t k_desc0 = smem_desc(sK(0), 16, 1024);
-        const uint64_t v_desc0 = smem_desc(sV(0), kSubBytes, 1024);
+        // V (MN-major): the next 64 columns of d are one sub-tile further on;
+        // with the ones column, the ones tile (slot s: its start field is 1024 s
+        // further on, its group stride 1024 s shorter)
+        const uint64_t v_desc0 =
+            C::kOnes ? smem_desc(sV(0), C::kOffOnes - C::kOffV, 1024) : smem_desc(sV(0), kSubBytes, 1024);
         // S_x = Q_x K_s^T into TMEM columns [128 x, 128 x + 128)
         auto issue_s = [&](int x, int s) {
             const uint64_t qd = q_desc0 + x * kTileStep, kd = k_desc0 + s * kTileStep;
@@ -447,8 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // K-steps of 16 each): the first half runs while the softmax warps
         // still compute the weights of the second
         auto issue_pv = [&](int x, int s, int half, bool acc) {
-            ptx::mma_ts_k64(tmem + kTmemU + x * 128, tmem + x * 128 + half * 32,
-                            v_desc0 + s * kTileStep + half * 512, idesc_pv, acc ? 1u : 0u);
+            const uint64_t vd = C::kOnes ? v_desc0 + s * kTileStep - ((s * kTileStep) << 16)
+                                         : v_desc0 + s * kTileStep;
+            ptx::mma_ts_k64(tmem + kTmemU + x * 128, tmem + x * 128 + half * 32, vd + half * 512,
+                            idesc_pv, acc ? 1u : 0u);
         };
         // both halves of P_x V_s for the n-th key tile of query tile x, each
         // issued once the softmax warps have written its weights; o_half /
@@ -585,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 pw = make_float2(ptx::ex2_approx(e.x), ptx::ex2_approx(e.y));
                 rs[c & 1] = __fadd2_rn(rs[c & 1], pw);
                 pk[c] = pack2<BF16>(pw.x, pw.y);
-                add_packed<BF16>(rh[c & 1], pk[c]);
+                if constexpr (!C::kOnes) add_packed<BF16>(rh[c & 1], pk[c]);  // else P.V sums them
             }
         };
         // scores [32 c, 32 c + 32) of this row, masked like load_scores
@@ -752,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const float2 av = make_float2(alpha, alpha);
 #pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {
+                    for (int c = 0; c < C::kUCols / 16; ++c) {  // with the sum column, if any
                         uint32_t ov[16];
                         ptx::tmem_ld_32x32b_x16(u_addr + c * 16, ov);
                         ptx::tmem_wait_ld();
@@ -781,7 +803,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!aborted && T > 0) aborted = !wait_warp(bar_o(x), (n - 1) & 1, abort, tmo);
             if (aborted) break;
             const float l_all = lsum.x + lsum.y;
-            const float lhat_all = lhat.x + lhat.y;
+            float lhat_all = lhat.x + lhat.y;
+            if constexpr (C::kOnes) {
+                // the sum of the 16-bit weights is U's column 64 (warp-uniform
+                // branch around the collective load)
+                lhat_all = 0.f;
+                if (T > 0) {
+                    ptx::tc_fence_after_sync();
+                    uint32_t lv = ptx::tmem_ld_32x32b_x1(u_addr + D);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence(lv);
+                    lhat_all = __uint_as_float(lv);
+                }
+            }
             if constexpr (SPLIT) {
                 // partial result of this key range: O normalised by its own lhat
                 // (fp32) and the two log-sums that weight it in the merge
