@@ -466,24 +466,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // U_x (+)= P_x V_s, P_x read from TMEM, in two halves of 64 keys (4
         // K-steps of 16 each): the first half runs while the softmax warps
         // still compute the weights of the second
-        auto issue_pv = [&](int x, int s, int half, bool acc) {
-            const uint64_t vd = C::kOnes ? v_desc0 + s * kTileStep - ((s * kTileStep) << 16)
-                                         : v_desc0 + s * kTileStep;
-            ptx::mma_ts_k64(tmem + kTmemU + x * 128, tmem + x * 128 + half * 32, vd + half * 512,
-                            idesc_pv, acc ? 1u : 0u);
-        };
         // both halves of P_x V_s for the n-th key tile of query tile x, each
         // issued once the softmax warps have written its weights; o_half /
-        // o_ready signal that U_x absorbed them
+        // o_ready signal that U_x absorbed them.  Everything but the products
+        // is computed before the waits: the issuer shares its sub-partition
+        // with two softmax warps, so each instruction between a barrier and
+        // the product it releases delays the tensor core.
         auto pv_tile = [&](int x, int s, uint32_t n, bool acc) {
-            if (!wait_warp(bar_ph(x), n & 1, abort, tmo)) return false;
+            const uint64_t vd = C::kOnes ? v_desc0 + s * kTileStep - ((s * kTileStep) << 16)
+                                         : v_desc0 + s * kTileStep;
+            const uint32_t d_u = tmem + kTmemU + x * 128, a_p = tmem + x * 128;
+            const uint32_t b_ph = bar_ph(x), b_pf = bar_pf(x), b_oh = bar_oh(x), b_o = bar_o(x);
+            const uint32_t par = n & 1, acc0 = acc ? 1u : 0u;
+            if (!wait_warp(b_ph, par, abort, tmo)) return false;
             ptx::tc_fence_after_sync();
-            issue_pv(x, s, 0, acc);
-            ptx::tc_commit_elect(bar_oh(x));
-            if (!wait_warp(bar_pf(x), n & 1, abort, tmo)) return false;
+            ptx::mma_ts_k64(d_u, a_p, vd, idesc_pv, acc0);
+            ptx::tc_commit_elect(b_oh);
+            if (!wait_warp(b_pf, par, abort, tmo)) return false;
             ptx::tc_fence_after_sync();
-            issue_pv(x, s, 1, true);
-            ptx::tc_commit_elect(bar_o(x));
+            ptx::mma_ts_k64(d_u, a_p + 32, vd + 512, idesc_pv, 1u);
+            ptx::tc_commit_elect(b_o);
             return true;
         };
         uint32_t kc = 0, vc = 0;    // K and V tiles consumed so far (same order as loaded)
@@ -517,15 +519,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < w.nB; ++j) {
                 const int sv = vc % NV;
                 const int sk = kc % NK;
+                // V_j, and with a ring of four K tiles K_{j+1} for the next S
+                // products: it was loaded long before, and waiting for it here
+                // keeps the wait off the path from a softmax signal to the
+                // product it releases.  With two K tiles it may still be on its
+                // way, and is only waited for just before the first S needs it.
+                constexpr bool kEarlyK = NK >= 4;
                 bool k_ready = false;
                 if (!(ok = wait_warp(bar_vf(sv), (vc / NV) & 1, abort, tmo))) break;
+                if (kEarlyK && j + 1 < w.nB) {
+                    if (!(ok = wait_warp(bar_kf(sk), (kc / NK) & 1, abort, tmo))) break;
+                    k_ready = true;
+                }
                 if (j < w.nA) {
                     // the first product of a unit overwrites U_x; the softmax
                     // warps read the previous unit's U_x before they signal P
                     if (!(ok = pv_tile(0, sv, na, j > 0))) break;
                     ++na;
                     if (j + 1 < w.nA) {
-                        if (!(ok = wait_warp(bar_kf(sk), (kc / NK) & 1, abort, tmo))) break;
+                        if (!k_ready && !(ok = wait_warp(bar_kf(sk), (kc / NK) & 1, abort, tmo))) break;
                         k_ready = true;
                         ptx::tc_fence_after_sync();
                         issue_s(0, sk);
