@@ -162,18 +162,24 @@ KernelEntry select_kernel(int kd, Kind k, int dtype, bool causal, bool split) {
 }
 
 template <int D>
-const void* merge_fn(bool bf) {
-    return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, true>)
-              : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, false>);
+const void* merge_fn(bool bf, int num_splits) {
+    if (num_splits <= 2)
+        return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, true, 2>)
+                  : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, false, 2>);
+    if (num_splits <= 4)
+        return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, true, 4>)
+                  : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, false, 4>);
+    return bf ? reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, true, 8>)
+              : reinterpret_cast<const void*>(&fa::fa_split_merge_kernel<D, false, 8>);
 }
 
-const void* select_merge(int kd, int dtype) {
+const void* select_merge(int kd, int dtype, int num_splits) {
     const bool bf = dtype == FA_BF16;
     switch (kd) {
-        case 64: return merge_fn<64>(bf);
-        case 128: return merge_fn<128>(bf);
-        case 192: return merge_fn<192>(bf);
-        default: return merge_fn<256>(bf);
+        case 64: return merge_fn<64>(bf, num_splits);
+        case 128: return merge_fn<128>(bf, num_splits);
+        case 192: return merge_fn<192>(bf, num_splits);
+        default: return merge_fn<256>(bf, num_splits);
     }
 }
 
@@ -388,7 +394,7 @@ int fwd_core(const fa_fwd_args& a, int fault_mode, double timeout_s) {
         mcfg.stream = st;
         mcfg.attrs = attr;
         mcfg.numAttrs = 1;
-        if (cudaLaunchKernelExC(&mcfg, select_merge(kd, dtype), margs) != cudaSuccess) return FA_ERR_CUDA;
+        if (cudaLaunchKernelExC(&mcfg, select_merge(kd, dtype, num_splits), margs) != cudaSuccess) return FA_ERR_CUDA;
     }
     return FA_OK;
 }

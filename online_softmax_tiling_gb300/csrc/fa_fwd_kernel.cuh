@@ -949,8 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // fed to P.V.  A warp per row; each lane owns D/32 consecutive columns of the
 // kernel's width D, of which the first d_out are written.  The merge is bound
 // by memory latency, not bandwidth, so a row's loads are issued before any is
-// used: lane s reads range s's two log-sums (one round trip for all ranges),
-// and the partial O rows are read four ranges at a time.
+// used: lane s reads range s's two log-sums while the partial O rows of up to
+// eight ranges are read, all in one round trip.
 struct MergeParams {
     const float* o_part;
     const float* lse_part;
@@ -976,10 +976,12 @@ __device__ __forceinline__ float lanes_sum(float v, int n) {
     return __shfl_sync(0xffffffffu, v, 0);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, int kBatch>
 __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams mp) {
+    // kBatch: ranges whose partial rows are in flight together (2, 4 or 8: the
+    // range count rounded up, so that few ranges keep few registers and many
+    // resident warps, which the larger partials of few ranges need)
     constexpr int kPer = D / 32;
-    constexpr int kBatch = 4;  // ranges whose partial rows are in flight together
     // launched as a programmatic dependent of the attention kernel: wait until
     // that grid has finished and its partials are visible (no-op otherwise)
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1003,26 +1005,17 @@ __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams m
     const unsigned hu = static_cast<unsigned>(mp.H), bu = static_cast<unsigned>(bh) / hu;  // BH < 2^31
     const long long b = bu, h = static_cast<unsigned>(bh) - bu * hu;
     const size_t plane = static_cast<size_t>(num_splits) * rows;
-    const float ls = lane < num_splits ? mp.lse_part[lane * rows + r] : -INFINITY;
-    const float lh = lane < num_splits ? mp.lse_part[plane + lane * rows + r] : -INFINITY;
-    const float ml = lanes_max(ls, num_splits), mh = lanes_max(lh, num_splits);
-    // an empty range (-inf) has no weight and wrote no O row
-    const float lsum = lanes_sum(ls == -INFINITY ? 0.f : __expf(ls - ml), num_splits);
-    const float w = lh == -INFINITY ? 0.f : __expf(lh - mh);
-    const float wsum = lanes_sum(w, num_splits);
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
     const float* src = mp.o_part + r * D + lane * kPer;
-    for (int s0 = 0; s0 < num_splits; s0 += kBatch) {
-        float ws[kBatch], v[kBatch][kPer];
+    // the partial rows of up to kBatch ranges, loaded whatever their weight
+    // (they do not depend on it): with the log-sums below, one round trip to
+    // memory for the row.  A range with no weight wrote no row; its stale
+    // values are dropped by selection, never multiplied by zero.
+    auto load_batch = [&](int s0, float (&v)[kBatch][kPer]) {
 #pragma unroll
         for (int j = 0; j < kBatch; ++j) {
-            const float wj = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);
-            ws[j] = s0 + j < num_splits ? wj : 0.f;
 #pragma unroll
             for (int e = 0; e < kPer; ++e) v[j][e] = 0.f;
-            if (ws[j] > 0.f) {
+            if (s0 + j < num_splits) {
                 const float* row_s = src + static_cast<size_t>(s0 + j) * rows * D;
                 if constexpr (kPer % 4 == 0) {
 #pragma unroll
@@ -1039,10 +1032,28 @@ __global__ void __launch_bounds__(256) fa_split_merge_kernel(const MergeParams m
                 }
             }
         }
+    };
+    float v[kBatch][kPer];
+    load_batch(0, v);
+    const float ls = lane < num_splits ? mp.lse_part[lane * rows + r] : -INFINITY;
+    const float lh = lane < num_splits ? mp.lse_part[plane + lane * rows + r] : -INFINITY;
+    const float ml = lanes_max(ls, num_splits), mh = lanes_max(lh, num_splits);
+    // an empty range (-inf) has no weight and wrote no O row
+    const float lsum = lanes_sum(ls == -INFINITY ? 0.f : __expf(ls - ml), num_splits);
+    const float w = lh == -INFINITY ? 0.f : __expf(lh - mh);
+    const float wsum = lanes_sum(w, num_splits);
+    float acc[kPer];
 #pragma unroll
-        for (int j = 0; j < kBatch; ++j)
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    for (int s0 = 0; s0 < num_splits; s0 += kBatch) {
+        if (s0 > 0) load_batch(s0, v);
 #pragma unroll
-            for (int e = 0; e < kPer; ++e) acc[e] = fmaf(ws[j], v[j][e], acc[e]);
+        for (int j = 0; j < kBatch; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);
+            const bool use = s0 + j < num_splits && wj > 0.f;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] = use ? fmaf(wj, v[j][e], acc[e]) : acc[e];
+        }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint32_t packed[kPer / 2];
