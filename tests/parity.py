@@ -147,7 +147,10 @@ def run_gpu(q_bits, k_bits, v_bits, dtype, scale, causal, guard: int = 0, num_sp
     else:
         s_eff = num_splits or fa.fa_splitkv_num_splits(B, H, N, d, int(causal))
         nbytes = max(fa.fa_splitkv_workspace_size(B, H, N, d, s_eff), 256)
-        ws = torch.full((nbytes + 2 * guard,), 0x7F, dtype=torch.uint8, device="cuda")
+        # NaN bit patterns: a range with no key for a row writes no partial
+        # row, so a merge that used such a stale row (even times a zero
+        # weight) would turn the output into NaN
+        ws = torch.full((nbytes + 2 * guard,), 0xFF, dtype=torch.uint8, device="cuda")
         st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                lse.data_ptr(), B, H, N, d, scale, int(causal), dtype, num_splits,
                                ws.data_ptr(), nbytes, stream.cuda_stream)
