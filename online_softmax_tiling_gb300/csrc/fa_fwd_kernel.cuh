@@ -395,13 +395,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b_idx = w.bh / p.H, h_idx = w.bh % p.H;
             if (nq > 0 && !(ok = wait_warp(bar_qe, (nq - 1) & 1, abort, tmo))) break;
             if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+                if constexpr (SPLIT) {
+                    // (the other key ranges of the block read the same Q)
+                    ptx::mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
 #pragma unroll
-                for (int x = 0; x < 2; ++x)
+                    for (int x = 0; x < 2; ++x)
 #pragma unroll
-                    for (int c = 0; c < C::kSub; ++c)
-                        ptx::tma_load_4d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
-                                         w.qb * kBlockM + x * kTileM, h_idx, b_idx);
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
+                                             w.qb * kBlockM + x * kTileM, h_idx, b_idx);
+                } else {
+                    // Q is read by this unit only: evicted first from L2, ahead of
+                    // the K and V lines the other query blocks of its head read
+                    const uint64_t pol_q = ptx::l2_policy_evict_first();
+                    ptx::mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+#pragma unroll
+                        for (int c = 0; c < C::kSub; ++c)
+                            ptx::tma_load_4d_hint(sQ(x) + c * kSubBytes, &tm_q, bar_q, 64 * c,
+                                                  w.qb * kBlockM + x * kTileM, h_idx, b_idx, pol_q);
+                }
             }
             ++nq;
             for (int j = 0; j <= w.nB; ++j) {
@@ -920,7 +934,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && !*abort) {
-                        ptx::tma_store_4d(&tm_o, stage, 64 * h, first_row + 32 * (warp & 3), h_idx, b_idx);
+                        // O is written once: its lines leave L2 first
+                        ptx::tma_store_4d_hint(&tm_o, stage, 64 * h, first_row + 32 * (warp & 3), h_idx,
+                                               b_idx, ptx::l2_policy_evict_first());
                         ptx::bulk_commit_group();
                     }
                 }
