@@ -57,3 +57,17 @@ def test_sweep_lists_every_config():
         assert any(n.startswith(cfg + "_") for n in names)
     assert "T_b2h32n4096d128_fp16" in names and "T_b2h32n4096d128_bf16" in names
     assert math.isclose(synth.workload("C3").flops, 4 * 4 * 16 * 4096 ** 2 * 64 / 2)
+
+
+def test_default_workload_has_traffic_for_the_current_sources():
+    """The committed ncu summaries carry a DRAM-traffic line for the default
+    workload under the hash of the kernel sources as they stand, so that the
+    default bench line's roofline.traffic is a measured figure, not null.  A
+    change to any hashed source needs a new capture."""
+    w = synth.workload(bench.DEFAULT_WORKLOAD)
+    traffic = bench.profiled_traffic(w.name, bench.kernel_hash("fused"))
+    assert traffic is not None, f"no capture for {w.name} under {bench.kernel_hash('fused')}"
+    # bytes of one launch: at least the compulsory reads of Q, K, V, and not
+    # far above the compulsory bytes (re-reads of K and V hit L2)
+    qkv = 3 * w.B * w.H * w.N * w.d * 2
+    assert qkv <= traffic <= 1.5 * w.compulsory_bytes
