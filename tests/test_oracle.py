@@ -31,13 +31,13 @@ def test_worked_example_recurrence_intermediates():
     ex = _ex()
     o, lse, tr = oracle.blocked_head(ex["Q"], ex["K"], ex["V"], ex["scale"], False,
                                      int(ex["block_n"]), trace=True)
-    # round 0 (Fig. 6, Fig. 8, l0 = 3/2, m = 1); no rescale on the first block
+    # key block 0 (Fig. 6, Fig. 8, l0 = 3/2, m = 1); no rescale on the first block
     np.testing.assert_allclose(tr["m"][0], ex["m0"], atol=EXACT)
     np.testing.assert_allclose(tr["e"][0], ex["E0"], atol=EXACT)
     np.testing.assert_allclose(tr["l"][0], ex["l0"], atol=EXACT)
     np.testing.assert_allclose(tr["u"][0], ex["U0"], atol=EXACT)
     assert np.all(np.isnan(tr["alpha"][0]))
-    # round 1 (alpha = 1/2, Fig. 7, l1, Fig. 9, Fig. 10)
+    # key block 1 (alpha = 1/2, Fig. 7, l1, Fig. 9, Fig. 10)
     np.testing.assert_allclose(tr["m"][1], ex["m1"], atol=EXACT)
     np.testing.assert_allclose(tr["alpha"][1], ex["alpha1"], atol=EXACT)
     np.testing.assert_allclose(tr["e"][1], ex["E1"], atol=EXACT)
